@@ -1,0 +1,156 @@
+/*
+ * gdg.h -- C ABI of the deterministic ragged BF16 grouped GEMM for B300 (sm_103a).
+ *
+ * The three operations are the rows of the computation table on the "Cake
+ * ragged BF16 grouped GEMM (experimental)" docs page; group e of the packed
+ * activations covers rows [s_e, t_e) as stated in that page's intro
+ * paragraph:
+ *
+ *   offs_kind == GDG_OFFS_ENDS   : offs[E] cumulative ends,  s_e = offs[e-1] (0 for e = 0), t_e = offs[e]
+ *   offs_kind == GDG_OFFS_INDPTR : m_indptr[E+1],            s_e = m_indptr[e], t_e = m_indptr[e+1]
+ *
+ *   fwd    Y[s_e:t_e]  = X[s_e:t_e] @ W[e]^T     X [rows,K], W [E,N,K] -> Y  [rows,N] bf16
+ *   dgrad  dX[s_e:t_e] = G[s_e:t_e] @ W[e]      G [rows,N], W [E,N,K] -> dX [rows,K] bf16
+ *   wgrad  dW[e]       = G[s_e:t_e]^T @ X[s_e:t_e]  G, X             -> dW [E,N,K] bf16 or fp32
+ *
+ * All operands are bf16, row-major and contiguous (last dimension has unit
+ * stride, rows are packed).  Products accumulate in fp32 on the tensor cores
+ * and every reduction runs in a fixed order with no atomics, so results are
+ * bitwise identical from run to run and independent of the GPU's SM count.
+ * An empty group gives a weight gradient of exactly +0.0.
+ *
+ * accumulate (wgrad only) follows the deterministic weight-gradient
+ * accumulation section of the MoE grouped GEMM pull request: out[e] +=
+ * G[e]^T X[e].  For an fp32 out the stored value is RN32(out + dW) with dW
+ * the fp32 weight gradient of the same call with accumulate = 0; for a bf16
+ * out it is bf16(float(out) + float(bf16(dW))).  Both are exactly the bits
+ * of out.add_(dW) in out's dtype.  The add is fused into the kernel's
+ * epilogue: no scratch copy of dW is made.
+ *
+ * Offsets live in DEVICE memory and are read only by the kernels: the host
+ * never synchronises on them.  Groups may be empty, a single row, or any
+ * size.  Offsets that are decreasing, negative or beyond rows are not
+ * detected (that would need a host sync); the kernels clamp every group to
+ * [0, rows] and treat a reversed range as empty, so such input gives
+ * unspecified values but never touches memory outside the given buffers.
+ * Rows outside every group are never written by fwd / dgrad and never read
+ * by wgrad ("row padding").
+ *
+ * Ownership: the caller owns every buffer (operands, out, offsets,
+ * workspace).  The library allocates no device memory, never synchronises
+ * the host, and launches only on the given stream.  Calls are stateless and
+ * may be captured in a CUDA graph; every launch or replay with accumulate
+ * adds again.  New offsets or values written into the same buffers are
+ * honoured by the next launch.
+ *
+ * Errors: every argument check runs on the host before anything is
+ * launched; on failure the call returns the status and launches nothing.
+ * Asynchronous kernel faults surface through the stream as usual.  Each
+ * in-kernel wait is bounded; a wait that runs out records GDG_ETIMEOUT in a
+ * device error word that gdg_device_error() returns.
+ */
+#ifndef GDG_H
+#define GDG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDG_API __attribute__((visibility("default")))
+#else
+#define GDG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdg_status {
+    GDG_OK = 0,
+    GDG_EINVAL = 1,     /* null pointer, E outside [1, GDG_MAX_EXPERTS], N/K <= 0, rows < 0,
+                           bad dtype or offs_kind, fwd/dgrad with fp32 out or accumulate,
+                           bad split_rows */
+    GDG_EALIGN = 2,     /* N % 256 or K % 64 != 0 (the stable grouped GEMM API's shape rule
+                           on the docs page), or a pointer not 16-byte aligned */
+    GDG_EOVERLAP = 3,   /* out shares a byte with an input or the offsets (the accumulate
+                           checks of the MoE grouped GEMM pull request) */
+    GDG_EWORKSPACE = 4, /* workspace missing or smaller than grouped_det_gemm_workspace_bytes */
+    GDG_ECUDA = 5,      /* a CUDA runtime or driver call failed (launch, tensor map encode) */
+    GDG_ETIMEOUT = 6    /* reported by gdg_device_error(): an in-kernel wait ran out */
+} gdg_status;
+
+typedef enum gdg_dtype { GDG_BF16 = 0, GDG_FP32 = 1 } gdg_dtype;
+
+typedef enum gdg_offs_kind { GDG_OFFS_ENDS = 0, GDG_OFFS_INDPTR = 1 } gdg_offs_kind;
+
+typedef enum gdg_op { GDG_OP_FWD = 0, GDG_OP_DGRAD = 1, GDG_OP_WGRAD = 2 } gdg_op;
+
+#define GDG_MAX_EXPERTS 1024
+
+/*
+ * Per-call buffers (all device pointers, 16-byte aligned):
+ *   fwd:   a = X [rows,K]   b = W [E,N,K]   out = Y  [rows,N] bf16
+ *   dgrad: a = G [rows,N]   b = W [E,N,K]   out = dX [rows,K] bf16
+ *   wgrad: a = G [rows,N]   b = X [rows,K]  out = dW [E,N,K] bf16 or fp32
+ * rows is the host-known number of packed rows (the operands' first
+ * dimension); the offsets must not point past it.
+ *
+ * split_rows (wgrad only; 0 for fwd/dgrad):
+ *    0  the library picks the form from the shapes alone (never from the SM count)
+ *   -1  one CTA reduces each output tile over all rows of its group
+ *   >0  (multiple of 64) every group's rows are cut into consecutive chunks of
+ *       split_rows rows; each chunk writes an fp32 partial tile into the
+ *       workspace and a second kernel adds the partials in chunk order
+ *       p0 + p1 + ... before rounding or accumulating.
+ * workspace / workspace_bytes: device scratch for the split form, at least
+ * grouped_det_gemm_workspace_bytes(...) bytes; ignored when that is 0.
+ */
+typedef struct gdg_args {
+    const void* a;
+    const void* b;
+    void* out;
+    void* workspace;
+    size_t workspace_bytes;
+    int64_t rows;
+    int32_t offs_kind;
+    int32_t split_rows;
+} gdg_args;
+
+/* Forward projection (docs page table, row "fwd"). out_dtype must be GDG_BF16 and
+ * accumulate 0.  rows == 0 launches nothing.  stream is a cudaStream_t (NULL = legacy
+ * default stream). */
+GDG_API gdg_status grouped_det_gemm_fwd(const gdg_args* args, const int32_t* offs, int E, int N, int K,
+                                gdg_dtype out_dtype, int accumulate, void* stream);
+
+/* Data gradient (docs page table, row "dgrad"; W used as stored, [N,K]).  Same rules
+ * as grouped_det_gemm_fwd. */
+GDG_API gdg_status grouped_det_gemm_dgrad(const gdg_args* args, const int32_t* offs, int E, int N,
+                                  int K, gdg_dtype out_dtype, int accumulate, void* stream);
+
+/* Weight gradient (docs page table, row "wgrad"; accumulate per the MoE grouped GEMM
+ * pull request).  Overwrite with rows == 0 writes +0.0 everywhere; accumulate with
+ * rows == 0 launches nothing and leaves out unchanged. */
+GDG_API gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int E, int N,
+                                  int K, gdg_dtype out_dtype, int accumulate, void* stream);
+
+/* Workspace bytes that grouped_det_gemm_<op> needs for these shapes and split_rows
+ * (0 unless op is GDG_OP_WGRAD and the split form is chosen).  (size_t)-1 for
+ * invalid arguments. */
+GDG_API size_t grouped_det_gemm_workspace_bytes(int op, int64_t rows, int E, int N, int K,
+                                        gdg_dtype out_dtype, int accumulate, int32_t split_rows);
+
+/* The split_rows value that split_rows == 0 resolves to for these shapes (-1 = unsplit). */
+GDG_API int32_t grouped_det_gemm_auto_split_rows(int64_t rows, int E, int N, int K);
+
+/* Static text for a status code. */
+GDG_API const char* gdg_status_string(gdg_status status);
+
+/* Synchronises the current device, returns the device error word (GDG_OK or
+ * GDG_ETIMEOUT) and clears it. */
+GDG_API gdg_status gdg_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDG_H */

@@ -1,0 +1,226 @@
+"""Deterministic ragged BF16 grouped GEMM for B300 -- Python binding of libgdg.so.
+
+The functions below carry the C ABI's names (include/gdg.h) and only marshal
+arguments: they read shapes and pointers off torch tensors, allocate missing
+outputs or workspace with torch, and pass everything to the CUDA library on
+the current stream.  All computation happens in the library's kernels.  There
+is no fallback: importing this package fails if libgdg.so is missing.
+
+Operations (computation table of the "Cake ragged BF16 grouped GEMM
+(experimental)" docs page; accumulate from the MoE grouped GEMM pull request):
+
+    grouped_det_gemm_fwd(x, w, offs)     Y[g]  = X[g] @ W[e].T   -> [rows, N] bf16
+    grouped_det_gemm_dgrad(g, w, offs)   dX[g] = G[g] @ W[e]     -> [rows, K] bf16
+    grouped_det_gemm_wgrad(g, x, offs)   dW[e] = G[g].T @ X[g]   -> [E, N, K] bf16/fp32
+                                        (accumulate=True: out[e] += G[g].T @ X[g])
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "GDG_OFFS_ENDS", "GDG_OFFS_INDPTR", "GDG_OP_FWD", "GDG_OP_DGRAD", "GDG_OP_WGRAD",
+    "GdgError", "grouped_det_gemm_fwd", "grouped_det_gemm_dgrad", "grouped_det_gemm_wgrad",
+    "grouped_det_gemm_workspace_bytes", "grouped_det_gemm_auto_split_rows",
+    "gdg_status_string", "gdg_device_error", "library_path",
+]
+
+GDG_OK, GDG_EINVAL, GDG_EALIGN, GDG_EOVERLAP, GDG_EWORKSPACE, GDG_ECUDA, GDG_ETIMEOUT = range(7)
+GDG_BF16, GDG_FP32 = 0, 1
+GDG_OFFS_ENDS, GDG_OFFS_INDPTR = 0, 1
+GDG_OP_FWD, GDG_OP_DGRAD, GDG_OP_WGRAD = 0, 1, 2
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdg.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is not built; run `python -m moe_ragged_bf16_grouped_b300.build`")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+
+class GdgArgs(ctypes.Structure):
+    _fields_ = [("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("rows", ctypes.c_int64), ("offs_kind", ctypes.c_int32),
+                ("split_rows", ctypes.c_int32)]
+
+
+for _name in ("grouped_det_gemm_fwd", "grouped_det_gemm_dgrad", "grouped_det_gemm_wgrad"):
+    _f = getattr(_lib, _name)
+    _f.restype = ctypes.c_int
+    _f.argtypes = [ctypes.POINTER(GdgArgs), ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+_lib.grouped_det_gemm_workspace_bytes.restype = ctypes.c_size_t
+_lib.grouped_det_gemm_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                                  ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int, ctypes.c_int32]
+_lib.grouped_det_gemm_auto_split_rows.restype = ctypes.c_int32
+_lib.grouped_det_gemm_auto_split_rows.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int]
+_lib.gdg_status_string.restype = ctypes.c_char_p
+_lib.gdg_status_string.argtypes = [ctypes.c_int]
+_lib.gdg_device_error.restype = ctypes.c_int
+_lib.gdg_device_error.argtypes = []
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+class GdgError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gdg_status_string(status)} (status {status})")
+
+
+def gdg_status_string(status: int) -> str:
+    return _lib.gdg_status_string(status).decode()
+
+
+def gdg_device_error() -> int:
+    """Synchronises the device and returns (and clears) the device error word."""
+    return _lib.gdg_device_error()
+
+
+def grouped_det_gemm_workspace_bytes(op: int, rows: int, E: int, N: int, K: int,
+                                     out_dtype: torch.dtype = torch.bfloat16,
+                                     accumulate: bool = False, split_rows: int = 0) -> int:
+    n = _lib.grouped_det_gemm_workspace_bytes(op, rows, E, N, K, _dtype_code(out_dtype),
+                                              int(accumulate), split_rows)
+    if n == ctypes.c_size_t(-1).value:
+        raise GdgError(GDG_EINVAL, "grouped_det_gemm_workspace_bytes")
+    return n
+
+
+def grouped_det_gemm_auto_split_rows(rows: int, E: int, N: int, K: int) -> int:
+    return _lib.grouped_det_gemm_auto_split_rows(rows, E, N, K)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return GDG_BF16
+    if dt == torch.float32:
+        return GDG_FP32
+    raise ValueError(f"unsupported output dtype {dt}")
+
+
+def _check_operand(t: torch.Tensor, name: str, dtype=torch.bfloat16, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _offs_kind(offs_kind) -> int:
+    if offs_kind in (GDG_OFFS_ENDS, "ends", "offs"):
+        return GDG_OFFS_ENDS
+    if offs_kind in (GDG_OFFS_INDPTR, "indptr", "m_indptr"):
+        return GDG_OFFS_INDPTR
+    raise ValueError(f"unknown offs_kind {offs_kind!r}")
+
+
+def _num_groups(offs: torch.Tensor, kind: int) -> int:
+    _check_operand(offs, "offs", torch.int32, 1)
+    return offs.numel() - (1 if kind == GDG_OFFS_INDPTR else 0)
+
+
+def _stream_ptr(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _call(fn, name, args, offs, E, N, K, dtype_code, accumulate, stream):
+    st = fn(ctypes.byref(args), offs.data_ptr(), E, N, K, dtype_code, accumulate, stream)
+    if st != GDG_OK:
+        raise GdgError(st, name)
+
+
+def grouped_det_gemm_fwd(x: torch.Tensor, w: torch.Tensor, offs: torch.Tensor,
+                         out: torch.Tensor | None = None, *, offs_kind=GDG_OFFS_ENDS,
+                         stream=None) -> torch.Tensor:
+    """Y[rows, N] with Y[g] = X[g] @ W[e].T for every group (rows outside all groups
+    are left as they are in ``out``)."""
+    kind = _offs_kind(offs_kind)
+    _check_operand(x, "x", ndim=2)
+    _check_operand(w, "w", ndim=3)
+    E, N, K = w.shape
+    if x.shape[1] != K or _num_groups(offs, kind) != E:
+        raise ValueError("shape mismatch between x, w and offs")
+    if out is None:
+        out = torch.empty((x.shape[0], N), dtype=torch.bfloat16, device=x.device)
+    _check_operand(out, "out", ndim=2)
+    if tuple(out.shape) != (x.shape[0], N):
+        raise ValueError("out must be [rows, N]")
+    args = GdgArgs(x.data_ptr(), w.data_ptr(), out.data_ptr(), None, 0, x.shape[0], kind, 0)
+    _call(_lib.grouped_det_gemm_fwd, "grouped_det_gemm_fwd", args, offs, E, N, K, GDG_BF16, 0,
+          _stream_ptr(stream, x.device))
+    return out
+
+
+def grouped_det_gemm_dgrad(g: torch.Tensor, w: torch.Tensor, offs: torch.Tensor,
+                           out: torch.Tensor | None = None, *, offs_kind=GDG_OFFS_ENDS,
+                           stream=None) -> torch.Tensor:
+    """dX[rows, K] with dX[g] = G[g] @ W[e] (W as stored)."""
+    kind = _offs_kind(offs_kind)
+    _check_operand(g, "g", ndim=2)
+    _check_operand(w, "w", ndim=3)
+    E, N, K = w.shape
+    if g.shape[1] != N or _num_groups(offs, kind) != E:
+        raise ValueError("shape mismatch between g, w and offs")
+    if out is None:
+        out = torch.empty((g.shape[0], K), dtype=torch.bfloat16, device=g.device)
+    _check_operand(out, "out", ndim=2)
+    if tuple(out.shape) != (g.shape[0], K):
+        raise ValueError("out must be [rows, K]")
+    args = GdgArgs(g.data_ptr(), w.data_ptr(), out.data_ptr(), None, 0, g.shape[0], kind, 0)
+    _call(_lib.grouped_det_gemm_dgrad, "grouped_det_gemm_dgrad", args, offs, E, N, K, GDG_BF16,
+          0, _stream_ptr(stream, g.device))
+    return out
+
+
+def grouped_det_gemm_wgrad(g: torch.Tensor, x: torch.Tensor, offs: torch.Tensor,
+                           out: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
+                           num_groups: int | None = None, *, accumulate: bool = False,
+                           split_rows: int = 0, workspace: torch.Tensor | None = None,
+                           offs_kind=GDG_OFFS_ENDS, stream=None) -> torch.Tensor:
+    """dW[E, N, K] with dW[e] = G[g].T @ X[g]; with ``accumulate`` the result is added
+    into ``out`` (bitwise ``out.add_(dW)`` in out's dtype)."""
+    kind = _offs_kind(offs_kind)
+    _check_operand(g, "g", ndim=2)
+    _check_operand(x, "x", ndim=2)
+    rows, N = g.shape
+    if x.shape[0] != rows:
+        raise ValueError("g and x must have the same number of rows")
+    K = x.shape[1]
+    E = _num_groups(offs, kind)
+    if num_groups is not None and num_groups != E:
+        raise ValueError("num_groups does not match offs")
+    if out is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs out")
+        out = torch.empty((E, N, K), dtype=out_dtype or torch.bfloat16, device=g.device)
+    if out_dtype is not None and out_dtype != out.dtype:
+        raise ValueError("out_dtype must be None or out.dtype")
+    _check_operand(out, "out", out.dtype, 3)
+    if tuple(out.shape) != (E, N, K):
+        raise ValueError("out must be [E, N, K]")
+    code = _dtype_code(out.dtype)
+    need = grouped_det_gemm_workspace_bytes(GDG_OP_WGRAD, rows, E, N, K, out.dtype, accumulate,
+                                            split_rows)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=g.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    args = GdgArgs(g.data_ptr(), x.data_ptr(), out.data_ptr(), ws_ptr, ws_bytes, rows, kind,
+                   split_rows)
+    _call(_lib.grouped_det_gemm_wgrad, "grouped_det_gemm_wgrad", args, offs, E, N, K, code,
+          int(accumulate), _stream_ptr(stream, g.device))
+    return out

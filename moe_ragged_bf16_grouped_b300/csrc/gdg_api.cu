@@ -1,0 +1,370 @@
+// Host side of the C ABI declared in include/gdg.h: argument checks, TMA tensor-map
+// encoding, form selection and kernel launches.  No device memory is allocated here and
+// the host never waits on the GPU (except in gdg_device_error, which says so).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gdg.h"
+#include "grouped_gemm.cuh"
+
+namespace {
+
+using gdg::GemmParams;
+using gdg::ReduceParams;
+
+__device__ unsigned int g_device_error = 0;
+
+constexpr int kMaxDevices = 64;
+
+// ------------------------------------------------------------------ driver entry point
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; OOB elements read as zero.
+bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+            const uint64_t* strides_bytes, const uint32_t* box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t d[3];
+    cuuint64_t s[2];
+    cuuint32_t b[3];
+    cuuint32_t es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
+    for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                    const_cast<void*>(base), d, s, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int cols, uint32_t box_rows) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(cols) * 2};
+    const uint32_t box[2] = {64, box_rows};
+    return encode(m, base, 2, dims, strides, box);
+}
+
+bool encode_weights(CUtensorMap* m, const void* base, int E, int N, int K, uint32_t box_n) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                              static_cast<uint64_t>(E)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2};
+    const uint32_t box[3] = {64, box_n, 1};
+    return encode(m, base, 3, dims, strides, box);
+}
+
+// ------------------------------------------------------------------ per-device caches
+
+struct DeviceInfo {
+    std::atomic<int> ready{0};
+    int sms = 0;
+    unsigned int* err = nullptr;
+    std::mutex mu;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+
+template <int OP>
+cudaError_t set_smem_attr() {
+    return cudaFuncSetAttribute(gdg::grouped_gemm_kernel<OP>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(gdg::kGemmSmemBytes));
+}
+
+// Per-device set-up, once: SM count, device error word address, kernel attributes.
+DeviceInfo* device_info(gdg_status* st) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *st = GDG_ECUDA;
+        return nullptr;
+    }
+    DeviceInfo& d = g_dev[dev];
+    if (d.ready.load(std::memory_order_acquire)) return &d;
+    std::lock_guard<std::mutex> lock(d.mu);
+    if (!d.ready.load(std::memory_order_relaxed)) {
+        void* err = nullptr;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaGetSymbolAddress(&err, g_device_error) != cudaSuccess ||
+            set_smem_attr<gdg::OP_FWD>() != cudaSuccess ||
+            set_smem_attr<gdg::OP_DGRAD>() != cudaSuccess ||
+            set_smem_attr<gdg::OP_WGRAD>() != cudaSuccess) {
+            *st = GDG_ECUDA;
+            return nullptr;
+        }
+        d.err = static_cast<unsigned int*>(err);
+        d.ready.store(1, std::memory_order_release);
+    }
+    return &d;
+}
+
+// ------------------------------------------------------------------ checks
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;   // [lo, hi)
+};
+
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+Range range_of(const void* p, uint64_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + static_cast<uintptr_t>(bytes)};
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int tiles_per_expert(int N, int K) {
+    return (N / gdg::kBM) * static_cast<int>(ceil_div(K, gdg::kBN));
+}
+
+int32_t auto_split_rows(int64_t rows, int E, int N, int K) {
+    const int64_t tpe = tiles_per_expert(N, K);
+    // Shapes with few output tiles leave SMs idle in the unsplit form; cut the rows of
+    // each group into fixed chunks instead.  The rule looks at shapes only, so the
+    // bits never depend on the GPU it runs on.
+    if (rows <= 0 || static_cast<int64_t>(E) * tpe >= 256) return -1;
+    int64_t r = ceil_div(rows * tpe, 512);
+    r = ceil_div(r, 64) * 64;
+    if (r < 128) r = 128;
+    if (r > (1 << 30)) r = 1 << 30;
+    return static_cast<int32_t>(r);
+}
+
+int64_t split_max_units(int64_t rows, int E, int N, int K, int32_t split_rows) {
+    return static_cast<int64_t>(tiles_per_expert(N, K)) * (ceil_div(rows, split_rows) + E);
+}
+
+gdg_status check_common(const gdg_args* args, const int32_t* offs, int E, int N, int K,
+                        gdg_dtype out_dtype) {
+    if (!args) return GDG_EINVAL;
+    if (E < 1 || E > GDG_MAX_EXPERTS || N <= 0 || K <= 0 || args->rows < 0 ||
+        args->rows > INT32_MAX - 1)
+        return GDG_EINVAL;
+    if (args->offs_kind != GDG_OFFS_ENDS && args->offs_kind != GDG_OFFS_INDPTR) return GDG_EINVAL;
+    if (out_dtype != GDG_BF16 && out_dtype != GDG_FP32) return GDG_EINVAL;
+    if (N % 256 != 0 || K % 64 != 0) return GDG_EALIGN;
+    if (static_cast<int64_t>(E) * N * K > (int64_t{1} << 40)) return GDG_EINVAL;
+    if (!offs) return GDG_EINVAL;
+    (void)offs;
+    return GDG_OK;
+}
+
+gdg_status launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return GDG_OK;
+    cudaGetLastError();   // clear a sticky launch-config error so later calls can proceed
+    return GDG_ECUDA;
+}
+
+// fwd (OP_FWD) and dgrad (OP_DGRAD) share everything but the operand maps.
+template <int OP>
+gdg_status run_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N, int K,
+                        gdg_dtype out_dtype, int accumulate, void* stream) {
+    gdg_status st = check_common(args, offs, E, N, K, out_dtype);
+    if (st != GDG_OK) return st;
+    if (out_dtype != GDG_BF16 || accumulate != 0 || args->split_rows != 0) return GDG_EINVAL;
+    const int64_t rows = args->rows;
+    if (rows == 0) return GDG_OK;
+    if (!args->a || !args->b || !args->out) return GDG_EINVAL;
+    if (!aligned16(args->a) || !aligned16(args->b) || !aligned16(args->out) || !aligned16(offs))
+        return GDG_EALIGN;
+    const int in_cols = (OP == gdg::OP_FWD) ? K : N;     // columns of the row operand
+    const int out_cols = (OP == gdg::OP_FWD) ? N : K;
+    const Range r_out = range_of(args->out, static_cast<uint64_t>(rows) * out_cols * 2);
+    const Range r_a = range_of(args->a, static_cast<uint64_t>(rows) * in_cols * 2);
+    const Range r_b = range_of(args->b, static_cast<uint64_t>(E) * N * K * 2);
+    const Range r_o = range_of(offs, static_cast<uint64_t>(E + args->offs_kind) * 4);
+    if (overlaps(r_out, r_a) || overlaps(r_out, r_b) || overlaps(r_out, r_o)) return GDG_EOVERLAP;
+
+    DeviceInfo* dev = device_info(&st);
+    if (!dev) return st;
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    if (!encode_weights(&p.tmA, args->b, E, N, K, OP == gdg::OP_FWD ? 128u : 64u))
+        return GDG_ECUDA;
+    for (int i = 0; i < 5; ++i)
+        if (!encode_rows(&p.tmB[i], args->a, rows, in_cols, 16u << i)) return GDG_ECUDA;
+    p.offs = offs;
+    p.out = args->out;
+    p.partial = nullptr;
+    p.err = dev->err;
+    p.rows = rows;
+    p.E = E;
+    p.N = N;
+    p.K = K;
+    p.offs_kind = args->offs_kind;
+    p.epi = gdg::EPI_BF16;
+    p.split_rows = 0;
+    const int64_t ft = (OP == gdg::OP_FWD) ? N / gdg::kBM : ceil_div(K, gdg::kBM);
+    const int64_t ub = ft * (ceil_div(rows, gdg::kRowTile) + E);
+    if (ub > INT32_MAX) return GDG_EINVAL;
+    p.max_units = static_cast<int>(ub);
+    const int grid = static_cast<int>(ub < dev->sms ? ub : dev->sms);
+    gdg::grouped_gemm_kernel<OP><<<grid, gdg::kThreads, gdg::kGemmSmemBytes,
+                                   static_cast<cudaStream_t>(stream)>>>(p);
+    return launch_status(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" {
+
+gdg_status grouped_det_gemm_fwd(const gdg_args* args, const int32_t* offs, int E, int N, int K,
+                                gdg_dtype out_dtype, int accumulate, void* stream) {
+    return run_fwd_like<gdg::OP_FWD>(args, offs, E, N, K, out_dtype, accumulate, stream);
+}
+
+gdg_status grouped_det_gemm_dgrad(const gdg_args* args, const int32_t* offs, int E, int N,
+                                  int K, gdg_dtype out_dtype, int accumulate, void* stream) {
+    return run_fwd_like<gdg::OP_DGRAD>(args, offs, E, N, K, out_dtype, accumulate, stream);
+}
+
+int32_t grouped_det_gemm_auto_split_rows(int64_t rows, int E, int N, int K) {
+    if (E < 1 || N <= 0 || K <= 0 || N % 256 || K % 64 || rows < 0) return -1;
+    return auto_split_rows(rows, E, N, K);
+}
+
+size_t grouped_det_gemm_workspace_bytes(int op, int64_t rows, int E, int N, int K,
+                                        gdg_dtype out_dtype, int accumulate, int32_t split_rows) {
+    if (E < 1 || E > GDG_MAX_EXPERTS || N <= 0 || K <= 0 || rows < 0 || N % 256 || K % 64 ||
+        (out_dtype != GDG_BF16 && out_dtype != GDG_FP32) || op < GDG_OP_FWD || op > GDG_OP_WGRAD)
+        return static_cast<size_t>(-1);
+    (void)accumulate;
+    if (op != GDG_OP_WGRAD) return 0;
+    if (split_rows == 0) split_rows = auto_split_rows(rows, E, N, K);
+    if (split_rows < 0 || rows == 0) return 0;
+    if (split_rows % 64 != 0) return static_cast<size_t>(-1);
+    return static_cast<size_t>(split_max_units(rows, E, N, K, split_rows)) * gdg::kPartialElems *
+           sizeof(float);
+}
+
+gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int E, int N,
+                                  int K, gdg_dtype out_dtype, int accumulate, void* stream) {
+    gdg_status st = check_common(args, offs, E, N, K, out_dtype);
+    if (st != GDG_OK) return st;
+    if (accumulate != 0 && accumulate != 1) return GDG_EINVAL;
+    int32_t split_rows = args->split_rows;
+    if (split_rows < -1 || (split_rows > 0 && split_rows % 64 != 0)) return GDG_EINVAL;
+    const int64_t rows = args->rows;
+    if (!args->out) return GDG_EINVAL;
+    if (rows > 0 && (!args->a || !args->b)) return GDG_EINVAL;
+    if (!aligned16(args->out) || !aligned16(offs) || (rows > 0 && (!aligned16(args->a) ||
+                                                                   !aligned16(args->b))))
+        return GDG_EALIGN;
+    const size_t osz = out_dtype == GDG_FP32 ? 4 : 2;
+    const Range r_out = range_of(args->out, static_cast<uint64_t>(E) * N * K * osz);
+    const Range r_a = range_of(args->a, static_cast<uint64_t>(rows) * N * 2);
+    const Range r_b = range_of(args->b, static_cast<uint64_t>(rows) * K * 2);
+    const Range r_o = range_of(offs, static_cast<uint64_t>(E + args->offs_kind) * 4);
+    if (overlaps(r_out, r_o) || (rows > 0 && (overlaps(r_out, r_a) || overlaps(r_out, r_b))))
+        return GDG_EOVERLAP;
+    if (rows == 0 && accumulate) return GDG_OK;   // nothing to add; out is left unchanged
+
+    if (split_rows == 0) split_rows = auto_split_rows(rows, E, N, K);
+    if (rows == 0) split_rows = -1;   // overwrite with no rows: the plain form writes +0.0
+    const bool split = split_rows > 0;
+    int64_t max_units = static_cast<int64_t>(E) * tiles_per_expert(N, K);
+    if (split) {
+        max_units = split_max_units(rows, E, N, K, split_rows);
+        const size_t need = static_cast<size_t>(max_units) * gdg::kPartialElems * sizeof(float);
+        if (!args->workspace || args->workspace_bytes < need) return GDG_EWORKSPACE;
+        if (!aligned16(args->workspace)) return GDG_EALIGN;
+        const Range r_w = range_of(args->workspace, need);
+        if (overlaps(r_w, r_out) || overlaps(r_w, r_o) ||
+            (rows > 0 && (overlaps(r_w, r_a) || overlaps(r_w, r_b))))
+            return GDG_EOVERLAP;
+    }
+    if (max_units > INT32_MAX) return GDG_EINVAL;
+
+    DeviceInfo* dev = device_info(&st);
+    if (!dev) return st;
+
+    const int epi = accumulate ? (out_dtype == GDG_FP32 ? gdg::EPI_FP32_ACC : gdg::EPI_BF16_ACC)
+                               : (out_dtype == GDG_FP32 ? gdg::EPI_FP32 : gdg::EPI_BF16);
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    // With rows == 0 no copy is ever issued; the maps still need a valid shape.
+    const int64_t map_rows = rows > 0 ? rows : 1;
+    const void* a = rows > 0 ? args->a : args->out;
+    const void* b = rows > 0 ? args->b : args->out;
+    if (!encode_rows(&p.tmA, a, map_rows, N, 64u) || !encode_rows(&p.tmB[0], b, map_rows, K, 64u))
+        return GDG_ECUDA;
+    p.offs = offs;
+    p.out = args->out;
+    p.partial = split ? static_cast<float*>(args->workspace) : nullptr;
+    p.err = dev->err;
+    p.rows = rows;
+    p.E = E;
+    p.N = N;
+    p.K = K;
+    p.offs_kind = args->offs_kind;
+    p.epi = split ? gdg::EPI_PARTIAL : epi;
+    p.split_rows = split ? split_rows : 0;
+    p.max_units = static_cast<int>(max_units);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int grid = static_cast<int>(max_units < dev->sms ? max_units : dev->sms);
+    gdg::grouped_gemm_kernel<gdg::OP_WGRAD><<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+    st = launch_status(cudaGetLastError());
+    if (st != GDG_OK || !split) return st;
+
+    ReduceParams r;
+    r.offs = offs;
+    r.partial = static_cast<const float*>(args->workspace);
+    r.out = args->out;
+    r.rows = rows;
+    r.E = E;
+    r.N = N;
+    r.K = K;
+    r.offs_kind = args->offs_kind;
+    r.epi = epi;
+    r.split_rows = split_rows;
+    r.max_units = static_cast<int>(max_units);
+    const int64_t vec4 = static_cast<int64_t>(E) * N * K / 4;
+    int64_t rgrid = ceil_div(vec4, gdg::kThreads);
+    if (rgrid > static_cast<int64_t>(dev->sms) * 8) rgrid = static_cast<int64_t>(dev->sms) * 8;
+    gdg::wgrad_reduce_kernel<<<static_cast<int>(rgrid), gdg::kThreads, 0, s>>>(r);
+    return launch_status(cudaGetLastError());
+}
+
+const char* gdg_status_string(gdg_status status) {
+    switch (status) {
+        case GDG_OK: return "ok";
+        case GDG_EINVAL: return "invalid argument";
+        case GDG_EALIGN: return "shape or alignment rule violated (N % 256, K % 64, 16-byte pointers)";
+        case GDG_EOVERLAP: return "output overlaps an input, the offsets or the workspace";
+        case GDG_EWORKSPACE: return "workspace missing or too small";
+        case GDG_ECUDA: return "CUDA call failed";
+        case GDG_ETIMEOUT: return "an in-kernel wait ran out";
+    }
+    return "unknown status";
+}
+
+gdg_status gdg_device_error(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return GDG_ECUDA;
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return GDG_ECUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess)
+        return GDG_ECUDA;
+    return v == 0 ? GDG_OK : GDG_ETIMEOUT;
+}
+
+}  // extern "C"

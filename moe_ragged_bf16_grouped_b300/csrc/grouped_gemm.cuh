@@ -1,0 +1,647 @@
+// Ragged BF16 grouped GEMM kernels for sm_103a: fwd, dgrad and wgrad (plain, fused
+// accumulate, or fixed split partials), plus the ordered reduce of those partials.
+//
+// Operations (computation table of the "Cake ragged BF16 grouped GEMM (experimental)"
+// docs page; group e = rows [s_e, t_e) of the packed operands, intro paragraph):
+//   fwd    Y[s_e:t_e]  = X[s_e:t_e] @ W[e]^T
+//   dgrad  dX[s_e:t_e] = G[s_e:t_e] @ W[e]
+//   wgrad  dW[e]       = G[s_e:t_e]^T @ X[s_e:t_e]
+//
+// Every kernel is persistent: one CTA per SM walks work units u = blockIdx.x,
+// blockIdx.x + gridDim.x, ...  The unit list is built on the device from the offsets
+// (no host sync): each CTA reads offs, counts the units of every group and takes an
+// exclusive prefix sum in shared memory; a binary search maps u back to its group.
+//
+// MMA orientation (tcgen05.mma, M = 128, N <= 256, K = 16 per instruction):
+//   fwd    D[n, row] = sum_k  W[e][n][k] * X[row][k]   A = W  K-major,  B = X  K-major
+//   dgrad  D[k, row] = sum_n  W[e][n][k] * G[row][n]   A = W  MN-major, B = G  K-major
+//   wgrad  D[n, k]   = sum_r  G[r][n]    * X[r][k]     A = G  MN-major, B = X  MN-major
+// For fwd / dgrad the packed rows are the MMA's N dimension, so a ragged group is
+// covered with 16-row granularity (N = round_up(rows in tile, 16)) instead of the
+// 128-row granularity of the M dimension; weights stream as the A operand.
+// For wgrad the reduction runs over the group's rows in 64-row stages starting exactly
+// at the group's first row; in the last stage the rows past the group end are zeroed
+// in shared memory and the MMAs past the last 16-row step are skipped.
+//
+// Warp roles (256 threads): warp 0 lane 0 issues TMA loads into a kStages-deep ring;
+// warp 1 lane 0 issues tcgen05.mma into one of two TMEM accumulators (2 x 256 fp32
+// columns); warp 2 owns the TMEM allocation; warps 4..7 drain TMEM (tcgen05.ld) and
+// write the outputs while the next tile's MMAs run into the other accumulator.
+//
+// Determinism: each output element is produced by exactly one CTA, whose MMA sequence
+// is fixed by the unit's coordinates alone (never by the grid size or timing); the
+// split form writes each partial once and the reduce adds partials in chunk order.
+// No atomics touch the data.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace gdg {
+
+constexpr int kBM = 128;                    // MMA M
+constexpr int kBN = 256;                    // MMA N (max)
+constexpr int kBK = 64;                     // reduction elements per stage (128 B of bf16)
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;      // 16 KB
+constexpr int kBBytes = kBN * kBK * 2;      // 32 KB
+constexpr int kBoxBytes = 64 * 128;         // one 64 x 64 bf16 TMA box
+constexpr int kThreads = 256;
+constexpr int kMaxE = 1024;
+constexpr int kTmemCols = 512;
+constexpr int kRowTile = 256;               // fwd / dgrad: packed rows per tile
+constexpr int kPartialElems = kBM * kBN;    // fp32 elements per split partial tile
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // any single wait > 2 s is a hang
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+
+enum Op : int { OP_FWD = 0, OP_DGRAD = 1, OP_WGRAD = 2 };
+enum Epi : int { EPI_BF16 = 0, EPI_FP32 = 1, EPI_BF16_ACC = 2, EPI_FP32_ACC = 3, EPI_PARTIAL = 4 };
+
+constexpr unsigned kDevErrTimeout = 6u;
+
+struct GemmParams {
+    CUtensorMap tmA;        // fwd: W box{64,128,1}; dgrad: W box{64,64,1}; wgrad: G box{64,64}
+    CUtensorMap tmB[5];     // fwd: X, dgrad: G, box{64, 16<<i}; wgrad: tmB[0] = X box{64,64}
+    const int32_t* offs;
+    void* out;
+    float* partial;         // wgrad split form: [max_units][128][256] fp32
+    unsigned int* err;      // device error word
+    int64_t rows;
+    int E, N, K;
+    int offs_kind;
+    int epi;
+    int split_rows;         // wgrad: > 0 selects the split form
+    int max_units;          // units at or past this index are skipped
+};
+
+struct SmemCtl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int total;
+    int warp_tot[kThreads / 32];
+    int start[kMaxE];
+    int size[kMaxE];
+    int prefix[kMaxE + 1];
+};
+
+constexpr size_t kGemmSmemBytes =
+    1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) + sizeof(SmemCtl);
+
+// ------------------------------------------------------------------ schedule
+
+struct Shape {
+    int ft;     // feature tiles (fwd, dgrad) or tiles per expert (wgrad)
+    int kt;     // wgrad: k tiles per expert
+};
+
+template <int OP>
+__device__ __forceinline__ Shape unit_shape(const GemmParams& p) {
+    Shape s;
+    if (OP == OP_FWD) { s.ft = p.N / kBM; s.kt = 1; }
+    else if (OP == OP_DGRAD) { s.ft = (p.K + kBM - 1) / kBM; s.kt = 1; }
+    else { s.kt = (p.K + kBN - 1) / kBN; s.ft = (p.N / kBM) * s.kt; }
+    return s;
+}
+
+// Rows [s, s + m) of group e, clamped to [0, rows]; a reversed range is empty.
+__device__ __forceinline__ void group_range(const int32_t* offs, int kind, int64_t rows, int e,
+                                            int& s, int& m) {
+    int64_t a, b;
+    if (kind == 0) { a = e > 0 ? offs[e - 1] : 0; b = offs[e]; }
+    else { a = offs[e]; b = offs[e + 1]; }
+    a = a < 0 ? 0 : (a > rows ? rows : a);
+    b = b < 0 ? 0 : (b > rows ? rows : b);
+    if (b < a) b = a;
+    s = static_cast<int>(a);
+    m = static_cast<int>(b - a);
+}
+
+template <int OP>
+__device__ __forceinline__ int units_of_group(int m, const Shape& sh, int split_rows) {
+    if (OP == OP_WGRAD) {
+        if (split_rows > 0) return ((m + split_rows - 1) / split_rows) * sh.ft;
+        return sh.ft;       // every tile of every expert, empty groups included
+    }
+    return ((m + kRowTile - 1) / kRowTile) * sh.ft;
+}
+
+// Builds start/size/prefix/total in shared memory.  Every thread of the block calls it.
+template <int OP>
+__device__ void build_schedule(const int32_t* offs, int kind, int64_t rows, int E,
+                               int split_rows, int max_units, const Shape& sh, int* start,
+                               int* size, int* prefix, int* warp_tot, int* total) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int v[4], local = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int e = tid * 4 + j;
+        v[j] = 0;
+        if (e < E) {
+            int s, m;
+            group_range(offs, kind, rows, e, s, m);
+            start[e] = s;
+            size[e] = m;
+            v[j] = units_of_group<OP>(m, sh, split_rows);
+        }
+        local += v[j];
+    }
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < kThreads / 32 ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < kThreads / 32) warp_tot[lane] = t;
+    }
+    __syncthreads();
+    int base = (warp ? warp_tot[warp - 1] : 0) + x - local;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int e = tid * 4 + j;
+        if (e < E) prefix[e] = base;
+        base += v[j];
+    }
+    if (tid == 0) {
+        const int tot = warp_tot[kThreads / 32 - 1];
+        prefix[E] = tot;
+        *total = tot < max_units ? tot : max_units;
+    }
+    __syncthreads();
+}
+
+// Largest e with prefix[e] <= u (prefix[0] == 0, non-decreasing).
+__device__ __forceinline__ int find_group(const int* prefix, int E, int u) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+struct Tile {
+    int e;
+    int f0;      // first M index (fwd: n, dgrad: k, wgrad: n)
+    int c0;      // first N index (fwd/dgrad: packed row, wgrad: k)
+    int ncols;   // valid N extent (<= 256)
+    int r0;      // wgrad: first reduction row
+    int nred;    // reduction length (fwd: K, dgrad: N, wgrad: rows of this unit)
+    int nkb;     // 64-wide reduction stages
+    int u;
+};
+
+template <int OP>
+__device__ __forceinline__ Tile decode_unit(const GemmParams& p, const SmemCtl* c,
+                                            const Shape& sh, int u) {
+    Tile t;
+    t.u = u;
+    t.e = find_group(c->prefix, p.E, u);
+    const int local = u - c->prefix[t.e];
+    const int s = c->start[t.e], m = c->size[t.e];
+    if (OP == OP_WGRAD) {
+        const int sp = local / sh.ft;
+        const int rem = local - sp * sh.ft;
+        const int nt = rem / sh.kt, kt = rem - nt * sh.kt;
+        t.f0 = nt * kBM;
+        t.c0 = kt * kBN;
+        t.ncols = min(kBN, p.K - t.c0);
+        if (p.split_rows > 0) {
+            t.r0 = s + sp * p.split_rows;
+            t.nred = min(p.split_rows, m - sp * p.split_rows);
+        } else {
+            t.r0 = s;
+            t.nred = m;
+        }
+    } else {
+        const int rc_n = (m + kRowTile - 1) / kRowTile;
+        const int ft = local / rc_n, rc = local - ft * rc_n;
+        t.f0 = ft * kBM;
+        t.c0 = s + rc * kRowTile;
+        t.ncols = min(kRowTile, m - rc * kRowTile);
+        t.r0 = 0;
+        t.nred = (OP == OP_FWD) ? p.K : p.N;
+    }
+    t.nkb = (t.nred + kBK - 1) / kBK;
+    return t;
+}
+
+// ------------------------------------------------------------------ waits
+
+// Bounded wait on an mbarrier phase.  Gives up when another role has aborted, or after
+// kWaitLimitNs, in which case it raises the abort flag and records a timeout.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SmemCtl* c,
+                                         unsigned int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*reinterpret_cast<volatile int*>(&c->abort_flag)) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *reinterpret_cast<volatile int*>(&c->abort_flag) = 1;
+            atomicCAS(err, 0u, kDevErrTimeout);
+            return false;
+        }
+    }
+}
+
+// Lane 0 waits (bounded); on success the other lanes then observe the completed phase
+// themselves, which cannot move on before this warp acts, so their waits return at once.
+__device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, SmemCtl* c,
+                                              unsigned int* err) {
+    const int lane = threadIdx.x & 31;
+    int ok = 1;
+    if (lane == 0) ok = wait_bar(bar, parity, c, err);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok && lane != 0) ok = wait_bar(bar, parity, c, err);
+    return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// Bounded wait that ignores the abort flag: used to let in-flight copies and MMAs land
+// before the CTA releases its shared memory and TMEM.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kDrainLimitNs) break;
+    }
+}
+
+// ------------------------------------------------------------------ epilogue helpers
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Writes 32 consecutive fp32 accumulator values of one dW row with the chosen epilogue.
+//   EPI_BF16     : dW = bf16_rn(acc)
+//   EPI_FP32     : dW = acc
+//   EPI_BF16_ACC : out = bf16_rn(float(out) + float(bf16_rn(acc)))   (bf16 out.add_(dW))
+//   EPI_FP32_ACC : out = out + acc, one fp32 RN add                   (fp32 out.add_(dW))
+//   EPI_PARTIAL  : fp32 partial tile row
+__device__ __forceinline__ void store_row32(int epi, void* dst_base, size_t off,
+                                            const uint32_t (&r)[32]) {
+    if (epi == EPI_BF16) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dst_base) + off);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
+            v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
+            v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
+            v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
+            dst[q] = v;
+        }
+    } else if (epi == EPI_BF16_ACC) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dst_base) + off);
+        uint4 old[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) old[q] = dst[q];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t o[4] = {old[q].x, old[q].y, old[q].z, old[q].w};
+            uint32_t nv[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const uint32_t d = pack_bf16x2(__uint_as_float(r[8 * q + 2 * h]),
+                                               __uint_as_float(r[8 * q + 2 * h + 1]));
+                nv[h] = pack_bf16x2(__fadd_rn(bf16_lo(o[h]), bf16_lo(d)),
+                                    __fadd_rn(bf16_hi(o[h]), bf16_hi(d)));
+            }
+            dst[q] = make_uint4(nv[0], nv[1], nv[2], nv[3]);
+        }
+    } else {
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(dst_base) + off);
+        if (epi == EPI_FP32_ACC) {
+            float4 old[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) old[q] = dst[q];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                dst[q] = make_float4(__fadd_rn(old[q].x, __uint_as_float(r[4 * q + 0])),
+                                     __fadd_rn(old[q].y, __uint_as_float(r[4 * q + 1])),
+                                     __fadd_rn(old[q].z, __uint_as_float(r[4 * q + 2])),
+                                     __fadd_rn(old[q].w, __uint_as_float(r[4 * q + 3])));
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
+                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        }
+    }
+}
+
+// ------------------------------------------------------------------ the GEMM kernel
+
+template <int OP>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + kStages * kABytes;
+    SmemCtl* c = reinterpret_cast<SmemCtl*>(sB + kStages * kBBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Shape sh = unit_shape<OP>(p);
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&c->full[s], 1);
+            mbar_init(&c->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&c->tfull[b], 1);
+            mbar_init(&c->tempty[b], 4 * 32);
+        }
+        mbar_init(&c->drain, 1);
+        c->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (tid == 32) {
+        prefetch_tmap(&p.tmA);
+        if (OP == OP_WGRAD) prefetch_tmap(&p.tmB[0]);
+        else
+            for (int i = 0; i < 5; ++i) prefetch_tmap(&p.tmB[i]);
+    }
+    if (warp == 2) {
+        tmem_alloc(&c->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    build_schedule<OP>(p.offs, p.offs_kind, p.rows, p.E, p.split_rows, p.max_units, sh,
+                       c->start, c->size, c->prefix, c->warp_tot, &c->total);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = c->tmem_base;
+    const int total = c->total;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, filled = 0, fill_parity = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+                const Tile t = decode_unit<OP>(p, c, sh, u);
+                int bi = 0;
+                if (OP != OP_WGRAD)
+                    while ((16 << bi) < t.ncols) ++bi;
+                for (int kb = 0; kb < t.nkb; ++kb) {
+                    if (!wait_bar(&c->empty[stage], phase ^ 1u, c, p.err)) { ok = false; break; }
+                    uint8_t* a = sA + stage * kABytes;
+                    uint8_t* b = sB + stage * kBBytes;
+                    uint64_t* fb = &c->full[stage];
+                    if (OP == OP_FWD) {
+                        mbar_arrive_expect_tx(fb, kABytes + (16u << bi) * 128u);
+                        tma_load_3d(a, &p.tmA, fb, kb * kBK, t.f0, t.e);
+                        tma_load_2d(b, &p.tmB[bi], fb, kb * kBK, t.c0);
+                    } else if (OP == OP_DGRAD) {
+                        const bool two = t.f0 + 64 < p.K;
+                        mbar_arrive_expect_tx(fb, (two ? 2u : 1u) * kBoxBytes + (16u << bi) * 128u);
+                        tma_load_3d(a, &p.tmA, fb, t.f0, kb * kBK, t.e);
+                        if (two) tma_load_3d(a + kBoxBytes, &p.tmA, fb, t.f0 + 64, kb * kBK, t.e);
+                        tma_load_2d(b, &p.tmB[bi], fb, kb * kBK, t.c0);
+                    } else {
+                        const int nb = t.ncols / 64;
+                        const int r = t.r0 + kb * kBK;
+                        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(2 + nb) * kBoxBytes);
+                        tma_load_2d(a, &p.tmA, fb, t.f0, r);
+                        tma_load_2d(a + kBoxBytes, &p.tmA, fb, t.f0 + 64, r);
+                        for (int j = 0; j < nb; ++j)
+                            tma_load_2d(b + j * kBoxBytes, &p.tmB[0], fb, t.c0 + 64 * j, r);
+                    }
+                    filled |= 1u << stage;
+                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // Let every copy this thread started land before the CTA exits.
+                for (int s = 0; s < kStages; ++s)
+                    if (filled & (1u << s)) drain_wait(&c->full[s], (fill_parity >> s) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        int stage = 0, it = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++it) {
+            const Tile t = decode_unit<OP>(p, c, sh, u);
+            const int buf = it & 1;
+            if (!wait_bar_warp(&c->tempty[buf], ((it >> 1) & 1) ^ 1u, c, p.err)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kBN);
+            const uint32_t n_mma = (OP == OP_WGRAD) ? static_cast<uint32_t>(t.ncols)
+                                                    : static_cast<uint32_t>((t.ncols + 15) & ~15);
+            const uint32_t idesc = idesc_bf16(kBM, n_mma, OP != OP_FWD, OP == OP_WGRAD);
+            for (int kb = 0; kb < t.nkb; ++kb) {
+                if (!wait_bar_warp(&c->full[stage], phase, c, p.err)) { ok = false; break; }
+                tc_fence_after();
+                uint8_t* a = sA + stage * kABytes;
+                uint8_t* b = sB + stage * kBBytes;
+                int nsteps = kBK / 16;
+                if (OP == OP_WGRAD) {
+                    const int valid = t.nred - kb * kBK;
+                    if (valid < kBK) {
+                        // Last stage of this unit: rows [valid, 16 * nsteps) of every box
+                        // hold rows of another group (or another split); zero them.  A whole
+                        // 128-byte row is zeroed, so the swizzle of its 16-byte chunks does
+                        // not matter.
+                        nsteps = (valid + 15) >> 4;
+                        const int zlo = valid * 128, zhi = nsteps * 16 * 128;
+                        const int chunks = (zhi - zlo) >> 4;
+                        const int nbox = 2 + t.ncols / 64;
+                        for (int i = lane; i < nbox * chunks; i += 32) {
+                            const int bx = i / chunks, ch = i - bx * chunks;
+                            uint8_t* base = bx < 2 ? a + bx * kBoxBytes : b + (bx - 2) * kBoxBytes;
+                            *reinterpret_cast<uint4*>(base + zlo + ch * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                }
+                if (lane == 0) {
+                    const uint32_t a_addr = smem_u32(a), b_addr = smem_u32(b);
+                    for (int kk = 0; kk < nsteps; ++kk) {
+                        const uint64_t ad = (OP == OP_FWD)
+                                                ? sdesc_sw128(a_addr + kk * 32, 16, 1024)
+                                                : sdesc_sw128(a_addr + kk * 2048, kBoxBytes, 1024);
+                        const uint64_t bd = (OP == OP_WGRAD)
+                                                ? sdesc_sw128(b_addr + kk * 2048, kBoxBytes, 1024)
+                                                : sdesc_sw128(b_addr + kk * 32, 16, 1024);
+                        umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                    }
+                    umma_commit(&c->empty[stage]);
+                }
+                __syncwarp();
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            if (lane == 0) {
+                if (t.nkb > 0) umma_commit(&c->tfull[buf]);
+                else mbar_arrive(&c->tfull[buf]);   // empty group: nothing to wait for
+            }
+            __syncwarp();
+        }
+        // Every MMA this thread issued has completed once this commit arrives.
+        if (lane == 0) {
+            umma_commit(&c->drain);
+            drain_wait(&c->drain, 0);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;                 // TMEM lanes [32q, 32q + 32)
+        int it = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+            const Tile t = decode_unit<OP>(p, c, sh, u);
+            const int buf = it & 1;
+            if (!wait_bar_warp(&c->tfull[buf], (it >> 1) & 1, c, p.err)) break;
+            tc_fence_after();
+            const int f = t.f0 + q * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(buf * kBN);
+            const int nchunks = (t.ncols + 31) >> 5;
+            for (int ch = 0; ch < nchunks; ++ch) {
+                uint32_t r[32];
+                if (t.nkb > 0) {
+                    tmem_ld_32x32b_x32(taddr + ch * 32, r);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = 0u;   // +0.0f
+                }
+                if (OP == OP_WGRAD) {
+                    if (p.epi == EPI_PARTIAL) {
+                        const size_t off = (static_cast<size_t>(t.u) * kBM + q * 32 + lane) * kBN + ch * 32;
+                        store_row32(EPI_FP32, p.partial, off, r);
+                    } else {
+                        const size_t off = (static_cast<size_t>(t.e) * p.N + f) * p.K + t.c0 + ch * 32;
+                        store_row32(p.epi, p.out, off, r);
+                    }
+                } else {
+                    const int fdim = (OP == OP_FWD) ? p.N : p.K;
+                    if (f < fdim) {
+                        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+                        const int jn = min(32, t.ncols - ch * 32);
+                        const int64_t row = t.c0 + ch * 32;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < jn)
+                                out[(row + j) * fdim + f] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&c->tempty[buf]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ ordered reduce
+
+struct ReduceParams {
+    const int32_t* offs;
+    const float* partial;
+    void* out;
+    int64_t rows;
+    int E, N, K;
+    int offs_kind;
+    int epi;            // EPI_BF16 / EPI_FP32 / EPI_BF16_ACC / EPI_FP32_ACC
+    int split_rows;
+    int max_units;
+};
+
+struct ReduceSmem {
+    int warp_tot[kThreads / 32];
+    int total;
+    int start[kMaxE];
+    int size[kMaxE];
+    int prefix[kMaxE + 1];
+};
+
+// dW[e][n][k] = p_0 + p_1 + ... + p_{S_e - 1} (fp32, left to right; +0.0 when S_e = 0),
+// then the same epilogue as the unsplit kernel.  4 consecutive k per thread.
+__global__ void __launch_bounds__(kThreads) wgrad_reduce_kernel(const __grid_constant__ ReduceParams p) {
+    __shared__ ReduceSmem sm;
+    Shape sh;
+    sh.kt = (p.K + kBN - 1) / kBN;
+    sh.ft = (p.N / kBM) * sh.kt;
+    build_schedule<OP_WGRAD>(p.offs, p.offs_kind, p.rows, p.E, p.split_rows, p.max_units, sh,
+                             sm.start, sm.size, sm.prefix, sm.warp_tot, &sm.total);
+    const int64_t NK = static_cast<int64_t>(p.N) * p.K;
+    const int64_t total4 = static_cast<int64_t>(p.E) * NK / 4;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total4;
+         i += static_cast<int64_t>(gridDim.x) * kThreads) {
+        const int64_t idx = i * 4;
+        const int e = static_cast<int>(idx / NK);
+        const int64_t rem = idx - e * NK;
+        const int n = static_cast<int>(rem / p.K);
+        const int k = static_cast<int>(rem - static_cast<int64_t>(n) * p.K);
+        const int S = (sm.size[e] + p.split_rows - 1) / p.split_rows;
+        const int tile = (n / kBM) * sh.kt + k / kBN;
+        const size_t within = static_cast<size_t>(n % kBM) * kBN + (k % kBN);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < S; ++s) {
+            const int u = sm.prefix[e] + s * sh.ft + tile;
+            if (u >= p.max_units) break;
+            const float4 v = *reinterpret_cast<const float4*>(
+                p.partial + static_cast<size_t>(u) * kPartialElems + within);
+            if (s == 0) acc = v;
+            else acc = make_float4(__fadd_rn(acc.x, v.x), __fadd_rn(acc.y, v.y),
+                                   __fadd_rn(acc.z, v.z), __fadd_rn(acc.w, v.w));
+        }
+        if (p.epi == EPI_FP32) {
+            reinterpret_cast<float4*>(p.out)[i] = acc;
+        } else if (p.epi == EPI_FP32_ACC) {
+            float4* o = reinterpret_cast<float4*>(p.out) + i;
+            const float4 old = *o;
+            *o = make_float4(__fadd_rn(old.x, acc.x), __fadd_rn(old.y, acc.y),
+                             __fadd_rn(old.z, acc.z), __fadd_rn(old.w, acc.w));
+        } else {
+            uint2* o = reinterpret_cast<uint2*>(p.out) + i;
+            uint2 d;
+            d.x = pack_bf16x2(acc.x, acc.y);
+            d.y = pack_bf16x2(acc.z, acc.w);
+            if (p.epi == EPI_BF16_ACC) {
+                const uint2 old = *o;
+                d.x = pack_bf16x2(__fadd_rn(bf16_lo(old.x), bf16_lo(d.x)),
+                                  __fadd_rn(bf16_hi(old.x), bf16_hi(d.x)));
+                d.y = pack_bf16x2(__fadd_rn(bf16_lo(old.y), bf16_lo(d.y)),
+                                  __fadd_rn(bf16_hi(old.y), bf16_hi(d.y)));
+            }
+            *o = d;
+        }
+    }
+}
+
+}  // namespace gdg

@@ -1,0 +1,132 @@
+"""C ABI checks that need no GPU: the library loads, exports every function that
+include/gdg.h declares, and refuses bad arguments on the host before any CUDA
+call (the checks of the accumulate section of the MoE grouped GEMM pull request
+run "before anything is allocated or bound")."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdg.h")
+LIB = os.path.join(ROOT, "moe_ragged_bf16_grouped_b300", "libgdg.so")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        from moe_ragged_bf16_grouped_b300 import build
+        build.build()
+    return ctypes.CDLL(LIB)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"GDG_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    assert {"grouped_det_gemm_fwd", "grouped_det_gemm_dgrad", "grouped_det_gemm_wgrad",
+            "grouped_det_gemm_workspace_bytes", "gdg_status_string"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+class Args(ctypes.Structure):
+    _fields_ = [("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("rows", ctypes.c_int64), ("offs_kind", ctypes.c_int32),
+                ("split_rows", ctypes.c_int32)]
+
+
+def call(lib, op, args, offs, E, N, K, dtype=0, acc=0):
+    f = getattr(lib, op)
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(Args), ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    return f(ctypes.byref(args) if args is not None else None, offs, E, N, K, dtype, acc, None)
+
+
+EINVAL, EALIGN, EOVERLAP, EWORKSPACE = 1, 2, 3, 4
+# Fake, 16-byte aligned device addresses: the host checks never dereference them.
+A, B, OUT, OFFS = 0x100000, 0x40000000, 0x80000000, 0xC0000000
+
+
+def good(rows=512, kind=0, split=0):
+    return Args(A, B, OUT, None, 0, rows, kind, split)
+
+
+@pytest.mark.parametrize("op", ["grouped_det_gemm_fwd", "grouped_det_gemm_dgrad",
+                                "grouped_det_gemm_wgrad"])
+def test_refusals_before_launch(lib, op):
+    assert call(lib, op, None, OFFS, 4, 256, 256) == EINVAL
+    assert call(lib, op, good(), None, 4, 256, 256) == EINVAL
+    assert call(lib, op, good(), OFFS, 0, 256, 256) == EINVAL
+    assert call(lib, op, good(), OFFS, 1025, 256, 256) == EINVAL
+    assert call(lib, op, good(rows=-1), OFFS, 4, 256, 256) == EINVAL
+    assert call(lib, op, good(kind=2), OFFS, 4, 256, 256) == EINVAL
+    assert call(lib, op, good(), OFFS, 4, 128, 256) == EALIGN      # N % 256
+    assert call(lib, op, good(), OFFS, 4, 256, 96) == EALIGN       # K % 64
+    assert call(lib, op, good(), OFFS, 4, 256, 256, dtype=7) == EINVAL
+    bad = good()
+    bad.out = OUT + 8
+    assert call(lib, op, bad, OFFS, 4, 256, 256) == EALIGN
+    ovl = good()
+    ovl.out = A + 4096                                             # inside the first operand
+    assert call(lib, op, ovl, OFFS, 4, 256, 256) == EOVERLAP
+
+
+def test_fwd_dgrad_refuse_fp32_and_accumulate(lib):
+    for op in ("grouped_det_gemm_fwd", "grouped_det_gemm_dgrad"):
+        assert call(lib, op, good(), OFFS, 4, 256, 256, dtype=1) == EINVAL
+        assert call(lib, op, good(), OFFS, 4, 256, 256, acc=1) == EINVAL
+        assert call(lib, op, good(split=64), OFFS, 4, 256, 256) == EINVAL
+
+
+def test_wgrad_refusals(lib):
+    op = "grouped_det_gemm_wgrad"
+    assert call(lib, op, good(split=100), OFFS, 4, 256, 256) == EINVAL      # not a multiple of 64
+    assert call(lib, op, good(split=-2), OFFS, 4, 256, 256) == EINVAL
+    assert call(lib, op, good(), OFFS, 4, 256, 256, acc=2) == EINVAL
+    assert call(lib, op, good(split=64), OFFS, 4, 256, 256) == EWORKSPACE   # split needs scratch
+    ovl = good()
+    ovl.out = OFFS - 64                                                     # dW covers the offsets
+    assert call(lib, op, ovl, OFFS, 4, 256, 256) == EOVERLAP
+    ws = good(split=64)
+    ws.workspace, ws.workspace_bytes = A + 4096, 1 << 30                    # scratch over an input
+    assert call(lib, op, ws, OFFS, 4, 256, 256) == EOVERLAP
+
+
+def test_workspace_bytes_and_auto_form(lib):
+    f = lib.grouped_det_gemm_workspace_bytes
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int32]
+    g = lib.grouped_det_gemm_auto_split_rows
+    g.restype = ctypes.c_int32
+    g.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    assert f(0, 512, 4, 256, 256, 0, 0, 0) == 0 and f(1, 512, 4, 256, 256, 0, 0, 0) == 0
+    assert f(2, 512, 4, 256, 256, 1, 0, -1) == 0
+    # split rows 64 on [E=4, N=256, K=256]: (N/128)*(K/256) = 2 tiles per expert,
+    # at most ceil(512/64) + 4 = 12 chunks -> 24 partial tiles of 128 x 256 fp32
+    assert f(2, 512, 4, 256, 256, 1, 1, 64) == 24 * 128 * 256 * 4
+    assert f(2, 512, 4, 256, 256, 0, 0, 100) == ctypes.c_size_t(-1).value
+    assert f(3, 512, 4, 256, 256, 0, 0, 0) == ctypes.c_size_t(-1).value
+    # the automatic form depends on shapes only
+    assert g(16384, 8, 14336, 4096) == -1          # many tiles: unsplit
+    assert g(65536, 64, 1536, 2048) == -1
+    r = g(512, 4, 256, 256)
+    assert r > 0 and r % 64 == 0
+    assert f(2, 512, 4, 256, 256, 0, 0, 0) == f(2, 512, 4, 256, 256, 0, 0, r)
+
+
+def test_status_strings(lib):
+    lib.gdg_status_string.restype = ctypes.c_char_p
+    for s in range(7):
+        assert lib.gdg_status_string(s)
+    assert b"unknown" in lib.gdg_status_string(99)
