@@ -54,6 +54,11 @@ def _load():
         f.argtypes = [u16p, u16p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                       ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
                       ctypes.c_void_p]
+        f = lib.gdg_oracle_wgrad_rows
+        f.restype = ctypes.c_int
+        f.argtypes = [u16p, u16p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                      ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
+                      ctypes.c_void_p]
         lib.gdg_oracle_bounds.restype = ctypes.c_int
         lib.gdg_oracle_bounds.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
@@ -183,4 +188,15 @@ def wgrad_entries(G, X, offs, E: int, N: int, K: int, flat_ids, kind: int = OFFS
     rows = g.shape[0]
     _check(_load().gdg_oracle_wgrad_entries(_ptr(g), _ptr(x), _ptr(o), kind, rows, E, N, K,
                                             _ptr(ids), len(ids), _ptr(vals)))
+    return vals
+
+
+def wgrad_rows(G, X, offs, E: int, N: int, K: int, pairs, kind: int = OFFS_ENDS):
+    """Whole rows dW[e, n, :] for the listed (e, n) pairs -> [len(pairs), K]."""
+    g, x, o = _bits(G), _bits(X), _offs(offs)
+    ids = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    vals = np.empty((len(ids), K))
+    rows = g.shape[0]
+    _check(_load().gdg_oracle_wgrad_rows(_ptr(g), _ptr(x), _ptr(o), kind, rows, E, N, K,
+                                         _ptr(ids), len(ids), _ptr(vals)))
     return vals

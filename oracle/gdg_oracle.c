@@ -201,6 +201,30 @@ int gdg_oracle_wgrad_entries(const uint16_t* G, const uint16_t* X, const int32_t
     return 0;
 }
 
+/* Whole dW rows dW[e, n, :] for the listed (e, n) pairs (pair j = ids[2j], ids[2j+1]);
+ * the same ascending-row sums as gdg_oracle_wgrad. */
+int gdg_oracle_wgrad_rows(const uint16_t* G, const uint16_t* X, const int32_t* offs,
+                          int offs_kind, int64_t rows, int E, int N, int K,
+                          const int64_t* ids, int64_t n_ids, double* vals) {
+    int64_t* st = (int64_t*)malloc(sizeof(int64_t) * 2 * (size_t)E);
+    if (!st) return -2;
+    int64_t* en = st + E;
+    if (gdg_oracle_bounds(offs, offs_kind, E, rows, st, en)) { free(st); return -1; }
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < n_ids; ++j) {
+        int e = (int)ids[2 * j], n = (int)ids[2 * j + 1];
+        double* out = vals + j * (int64_t)K;
+        for (int k = 0; k < K; ++k) out[k] = 0.0;
+        for (int64_t i = st[e]; i < en[e]; ++i) {
+            double g = bf16_to_double(G[i * (int64_t)N + n]);
+            const uint16_t* xr = X + i * (int64_t)K;
+            for (int k = 0; k < K; ++k) out[k] += g * bf16_to_double(xr[k]);
+        }
+    }
+    free(st);
+    return 0;
+}
+
 int gdg_oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

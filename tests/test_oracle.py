@@ -295,6 +295,9 @@ def test_sampled_forms_equal_full_forms():
     flat = np.random.default_rng(0).choice(dW.size, 200, replace=False)
     vals = oracle.wgrad_entries(G, X, offs, E, N, K, flat, wl.OFFS_INDPTR)
     assert np.array_equal(vals, dW.ravel()[flat])
+    pairs = [(e, n) for e in range(E) for n in (0, 5, N - 1)]
+    rows_w = oracle.wgrad_rows(G, X, offs, E, N, K, pairs, wl.OFFS_INDPTR)
+    assert np.array_equal(rows_w, np.stack([dW[e, n] for e, n in pairs]))
 
 
 # --------------------------------------------------------------------------
