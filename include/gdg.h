@@ -149,6 +149,42 @@ GDG_API const char* gdg_status_string(gdg_status status);
  * GDG_ETIMEOUT) and clears it. */
 GDG_API gdg_status gdg_device_error(void);
 
+/* Bytes of the library's own fixed scratch used by grouped_det_gemm_wgrad_noalloc. */
+#define GDG_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * Weight gradient for callers that cannot allocate device memory.  The pages have no
+ * counterpart of this entry point; it exists for this library's users.
+ *
+ * Some callers cannot call cudaMalloc at the point where they need a weight gradient:
+ * code running inside a memory pool or allocator that must not recurse into the driver,
+ * runtimes that own all device memory and hand out only the tensors of the step, or
+ * hosts where an allocation could block or fail at a bad moment.  The split form of
+ * grouped_det_gemm_wgrad needs fp32 scratch for its partial tiles, normally passed as
+ * args->workspace.  This variant uses instead one file-scope device array of
+ * GDG_NOALLOC_SCRATCH_BYTES bytes inside the library (every GPU that loads the library
+ * holds it until the process exits) and allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.  The caller still passes G, X, the offsets and out exactly as
+ * for grouped_det_gemm_wgrad; args->workspace and args->workspace_bytes are ignored.
+ *
+ * It always runs the split form: args->split_rows > 0 (a multiple of 64) is used as given;
+ * 0 takes the automatic value, or one chunk per group when the automatic rule picks the
+ * unsplit form; a negative value is refused with GDG_EINVAL.  A problem whose partials need
+ * more than GDG_NOALLOC_SCRATCH_BYTES (grouped_det_gemm_workspace_bytes for the resolved
+ * split_rows) is refused with GDG_EWORKSPACE and nothing is launched.  Results are bitwise
+ * equal to grouped_det_gemm_wgrad with the same split_rows.
+ *
+ * The first call on a device looks up the array's device address (once per device, with
+ * that device current); make that first call before any stream capture.  Every call shares
+ * the one array and it keeps the last call's partials; each call writes every partial tile
+ * it later reads, so nothing needs clearing between calls.  Calls whose kernels overlap on
+ * the GPU (other streams, other host threads) race on the array and give wrong results:
+ * serialise them.
+ */
+GDG_API gdg_status grouped_det_gemm_wgrad_noalloc(const gdg_args* args, const int32_t* offs,
+                                                  int E, int N, int K, gdg_dtype out_dtype,
+                                                  int accumulate, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

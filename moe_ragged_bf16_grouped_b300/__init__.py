@@ -25,6 +25,7 @@ __all__ = [
     "GDG_OFFS_ENDS", "GDG_OFFS_INDPTR", "GDG_OP_FWD", "GDG_OP_DGRAD", "GDG_OP_WGRAD",
     "GdgError", "grouped_det_gemm_fwd", "grouped_det_gemm_dgrad", "grouped_det_gemm_wgrad",
     "grouped_det_gemm_workspace_bytes", "grouped_det_gemm_auto_split_rows",
+    "grouped_det_gemm_wgrad_noalloc", "GDG_NOALLOC_SCRATCH_BYTES",
     "gdg_status_string", "gdg_device_error", "library_path",
 ]
 
@@ -32,6 +33,7 @@ GDG_OK, GDG_EINVAL, GDG_EALIGN, GDG_EOVERLAP, GDG_EWORKSPACE, GDG_ECUDA, GDG_ETI
 GDG_BF16, GDG_FP32 = 0, 1
 GDG_OFFS_ENDS, GDG_OFFS_INDPTR = 0, 1
 GDG_OP_FWD, GDG_OP_DGRAD, GDG_OP_WGRAD = 0, 1, 2
+GDG_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdg.so")
 if not os.path.exists(_LIB_PATH):
@@ -46,7 +48,8 @@ class GdgArgs(ctypes.Structure):
                 ("split_rows", ctypes.c_int32)]
 
 
-for _name in ("grouped_det_gemm_fwd", "grouped_det_gemm_dgrad", "grouped_det_gemm_wgrad"):
+for _name in ("grouped_det_gemm_fwd", "grouped_det_gemm_dgrad", "grouped_det_gemm_wgrad",
+              "grouped_det_gemm_wgrad_noalloc"):
     _f = getattr(_lib, _name)
     _f.restype = ctypes.c_int
     _f.argtypes = [ctypes.POINTER(GdgArgs), ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
@@ -223,4 +226,29 @@ def grouped_det_gemm_wgrad(g: torch.Tensor, x: torch.Tensor, offs: torch.Tensor,
                    split_rows)
     _call(_lib.grouped_det_gemm_wgrad, "grouped_det_gemm_wgrad", args, offs, E, N, K, code,
           int(accumulate), _stream_ptr(stream, g.device))
+    return out
+
+
+def grouped_det_gemm_wgrad_noalloc(g: torch.Tensor, x: torch.Tensor, offs: torch.Tensor,
+                                   out: torch.Tensor, *, accumulate: bool = False,
+                                   split_rows: int = 0, offs_kind=GDG_OFFS_ENDS,
+                                   stream=None) -> torch.Tensor:
+    """Split-form weight gradient into ``out`` using only the library's fixed device
+    scratch (GDG_NOALLOC_SCRATCH_BYTES) instead of a caller workspace: for callers that
+    must not allocate device memory while computing it.  ``out`` is required; nothing is
+    allocated here either.  Calls that overlap on the GPU share the scratch and race."""
+    kind = _offs_kind(offs_kind)
+    _check_operand(g, "g", ndim=2)
+    _check_operand(x, "x", ndim=2)
+    rows, N = g.shape
+    if x.shape[0] != rows:
+        raise ValueError("g and x must have the same number of rows")
+    K = x.shape[1]
+    E = _num_groups(offs, kind)
+    _check_operand(out, "out", out.dtype, 3)
+    if tuple(out.shape) != (E, N, K):
+        raise ValueError("out must be [E, N, K]")
+    args = GdgArgs(g.data_ptr(), x.data_ptr(), out.data_ptr(), None, 0, rows, kind, split_rows)
+    _call(_lib.grouped_det_gemm_wgrad_noalloc, "grouped_det_gemm_wgrad_noalloc", args, offs, E,
+          N, K, _dtype_code(out.dtype), int(accumulate), _stream_ptr(stream, g.device))
     return out

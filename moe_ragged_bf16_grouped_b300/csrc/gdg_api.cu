@@ -368,3 +368,75 @@ gdg_status gdg_device_error(void) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ fixed-scratch wgrad
+//
+// Scratch for the split partials of grouped_det_gemm_wgrad_noalloc, for callers that cannot
+// allocate device memory.  In host code the name below is only a host-side stand-in: its
+// device address comes from cudaGetSymbolAddress, once per device, with that device current.
+
+static __device__ __align__(256) float g_noalloc_scratch[GDG_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+
+struct NoAllocSlot {
+    std::atomic<void*> ptr{nullptr};
+    std::mutex mu;
+};
+
+NoAllocSlot g_noalloc[kMaxDevices];
+
+// Device address of g_noalloc_scratch on the current device (looked up on first use).
+void* noalloc_scratch(gdg_status* st) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *st = GDG_ECUDA;
+        return nullptr;
+    }
+    NoAllocSlot& slot = g_noalloc[dev];
+    void* p = slot.ptr.load(std::memory_order_acquire);
+    if (p) return p;
+    std::lock_guard<std::mutex> lock(slot.mu);
+    p = slot.ptr.load(std::memory_order_relaxed);
+    if (!p) {
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            *st = GDG_ECUDA;
+            return nullptr;
+        }
+        slot.ptr.store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+}  // namespace
+
+extern "C" gdg_status grouped_det_gemm_wgrad_noalloc(const gdg_args* args, const int32_t* offs,
+                                                     int E, int N, int K, gdg_dtype out_dtype,
+                                                     int accumulate, void* stream) {
+    if (!args || args->split_rows < 0) return GDG_EINVAL;
+    int32_t split_rows = args->split_rows;
+    if (split_rows == 0) {
+        split_rows = grouped_det_gemm_auto_split_rows(args->rows, E, N, K);
+        if (split_rows <= 0) {   // automatic rule picked the unsplit form: one chunk per group
+            const int64_t r = args->rows > 64 ? args->rows : 64;
+            if (r > (int64_t{1} << 30)) return GDG_EINVAL;
+            split_rows = static_cast<int32_t>((r + 63) / 64 * 64);
+        }
+    }
+    const size_t need = grouped_det_gemm_workspace_bytes(GDG_OP_WGRAD, args->rows, E, N, K,
+                                                         out_dtype, accumulate, split_rows);
+    if (need == static_cast<size_t>(-1)) return GDG_EINVAL;
+    if (need > GDG_NOALLOC_SCRATCH_BYTES) return GDG_EWORKSPACE;
+    gdg_args a = *args;
+    a.split_rows = split_rows;
+    a.workspace = nullptr;
+    a.workspace_bytes = 0;
+    if (need > 0) {
+        gdg_status st = GDG_OK;
+        a.workspace = noalloc_scratch(&st);
+        if (!a.workspace) return st;
+        a.workspace_bytes = GDG_NOALLOC_SCRATCH_BYTES;
+    }
+    return grouped_det_gemm_wgrad(&a, offs, E, N, K, out_dtype, accumulate, stream);
+}
