@@ -43,10 +43,10 @@ bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
             const uint64_t* strides_bytes, const uint32_t* box) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t d[3];
-    cuuint64_t s[2];
-    cuuint32_t b[3];
-    cuuint32_t es[3] = {1, 1, 1};
+    cuuint64_t d[4];
+    cuuint64_t s[3];
+    cuuint32_t b[4];
+    cuuint32_t es[4] = {1, 1, 1, 1};
     for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
     for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
@@ -69,6 +69,26 @@ bool encode_weights(CUtensorMap* m, const void* base, int E, int N, int K, uint3
     const uint64_t strides[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2};
     const uint32_t box[3] = {64, box_n, 1};
     return encode(m, base, 3, dims, strides, box);
+}
+
+// [rows, cols] bf16 seen as {64 columns, rows, cols/64 blocks}: one box {64, 64, nblk} brings
+// nblk 64-column blocks of 64 rows, each block a contiguous 8 KB in shared memory.
+bool encode_row_blocks(CUtensorMap* m, const void* base, int64_t rows, int cols, uint32_t nblk) {
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(rows), static_cast<uint64_t>(cols / 64)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(cols) * 2, 128};
+    const uint32_t box[3] = {64, 64, nblk};
+    return encode(m, base, 3, dims, strides, box);
+}
+
+// W [E, N, K] seen as {64 k, N, K/64 blocks, E}: box {64, 64, 2, 1} brings two 64-wide k blocks
+// of 64 n-rows of one expert.
+bool encode_weight_blocks(CUtensorMap* m, const void* base, int E, int N, int K) {
+    const uint64_t dims[4] = {64, static_cast<uint64_t>(N), static_cast<uint64_t>(K / 64),
+                              static_cast<uint64_t>(E)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(K) * 2, 128,
+                                 static_cast<uint64_t>(N) * K * 2};
+    const uint32_t box[4] = {64, 64, 2, 1};
+    return encode(m, base, 4, dims, strides, box);
 }
 
 // ------------------------------------------------------------------ per-device caches
@@ -199,7 +219,8 @@ gdg_status run_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N,
 
     GemmParams p;
     std::memset(&p, 0, sizeof p);
-    if (!encode_weights(&p.tmA, args->b, E, N, K, OP == gdg::OP_FWD ? 128u : 64u))
+    if (OP == gdg::OP_FWD ? !encode_weights(&p.tmA, args->b, E, N, K, 128u)
+                          : !encode_weight_blocks(&p.tmA, args->b, E, N, K))
         return GDG_ECUDA;
     for (int i = 0; i < 5; ++i)
         if (!encode_rows(&p.tmB[i], args->a, rows, in_cols, 16u << i)) return GDG_ECUDA;
@@ -306,7 +327,8 @@ gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int
     const int64_t map_rows = rows > 0 ? rows : 1;
     const void* a = rows > 0 ? args->a : args->out;
     const void* b = rows > 0 ? args->b : args->out;
-    if (!encode_rows(&p.tmA, a, map_rows, N, 64u) || !encode_rows(&p.tmB[0], b, map_rows, K, 64u))
+    if (!encode_row_blocks(&p.tmA, a, map_rows, N, 2u) ||
+        !encode_row_blocks(&p.tmB[0], b, map_rows, K, 4u))
         return GDG_ECUDA;
     p.offs = offs;
     p.out = args->out;

@@ -62,8 +62,10 @@ enum Epi : int { EPI_BF16 = 0, EPI_FP32 = 1, EPI_BF16_ACC = 2, EPI_FP32_ACC = 3,
 constexpr unsigned kDevErrTimeout = 6u;
 
 struct GemmParams {
-    CUtensorMap tmA;        // fwd: W box{64,128,1}; dgrad: W box{64,64,1}; wgrad: G box{64,64}
-    CUtensorMap tmB[5];     // fwd: X, dgrad: G, box{64, 16<<i}; wgrad: tmB[0] = X box{64,64}
+    CUtensorMap tmA;        // fwd: W box{64,128,1}; dgrad: W {k%64, n, k/64, e} box{64,64,2,1};
+                            // wgrad: G {n%64, row, n/64} box{64,64,2}
+    CUtensorMap tmB[5];     // fwd: X, dgrad: G, box{64, 16<<i}; wgrad: tmB[0] = X
+                            // {k%64, row, k/64} box{64,64,4}
     const int32_t* offs;
     void* out;
     float* partial;         // wgrad split form: [max_units][128][256] fp32
@@ -417,19 +419,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         tma_load_3d(a, &p.tmA, fb, kb * kBK, t.f0, t.e);
                         tma_load_2d(b, &p.tmB[bi], fb, kb * kBK, t.c0);
                     } else if (OP == OP_DGRAD) {
-                        const bool two = t.f0 + 64 < p.K;
-                        mbar_arrive_expect_tx(fb, (two ? 2u : 1u) * kBoxBytes + (16u << bi) * 128u);
-                        tma_load_3d(a, &p.tmA, fb, t.f0, kb * kBK, t.e);
-                        if (two) tma_load_3d(a + kBoxBytes, &p.tmA, fb, t.f0 + 64, kb * kBK, t.e);
+                        // One copy brings both 64-wide k blocks of W[e] (a block past K
+                        // reads as zeros): the map's third dimension walks the blocks.
+                        mbar_arrive_expect_tx(fb, 2u * kBoxBytes + (16u << bi) * 128u);
+                        tma_load_4d(a, &p.tmA, fb, 0, kb * kBK, t.f0 / 64, t.e);
                         tma_load_2d(b, &p.tmB[bi], fb, kb * kBK, t.c0);
                     } else {
-                        const int nb = t.ncols / 64;
+                        // One copy per operand: the maps' third dimension walks 64-column
+                        // blocks, so G's two blocks and X's four land as consecutive 8 KB
+                        // boxes (blocks past K read as zeros).
                         const int r = t.r0 + kb * kBK;
-                        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(2 + nb) * kBoxBytes);
-                        tma_load_2d(a, &p.tmA, fb, t.f0, r);
-                        tma_load_2d(a + kBoxBytes, &p.tmA, fb, t.f0 + 64, r);
-                        for (int j = 0; j < nb; ++j)
-                            tma_load_2d(b + j * kBoxBytes, &p.tmB[0], fb, t.c0 + 64 * j, r);
+                        mbar_arrive_expect_tx(fb, 6u * kBoxBytes);
+                        tma_load_3d(a, &p.tmA, fb, 0, r, t.f0 / 64);
+                        tma_load_3d(b, &p.tmB[0], fb, 0, r, t.c0 / 64);
                     }
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
