@@ -15,9 +15,6 @@ LIB = os.path.join(ROOT, "moe_ragged_bf16_grouped_b300", "libgdg.so")
 
 @pytest.fixture(scope="module")
 def lib():
-    if not os.path.exists(LIB):
-        from moe_ragged_bf16_grouped_b300 import build
-        build.build()
     return ctypes.CDLL(LIB)
 
 

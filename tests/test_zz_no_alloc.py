@@ -30,9 +30,6 @@ class Args(ctypes.Structure):
 
 
 def _fn():
-    if not os.path.exists(LIB):
-        from moe_ragged_bf16_grouped_b300 import build
-        build.build()
     f = ctypes.CDLL(LIB).grouped_det_gemm_wgrad_noalloc
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.POINTER(Args), ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
