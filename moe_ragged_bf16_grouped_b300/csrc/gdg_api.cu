@@ -56,38 +56,24 @@ bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
     return r == CUDA_SUCCESS;
 }
 
-bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int cols, uint32_t box_rows) {
-    const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(cols) * 2};
-    const uint32_t box[2] = {64, box_rows};
-    return encode(m, base, 2, dims, strides, box);
-}
-
-bool encode_weights(CUtensorMap* m, const void* base, int E, int N, int K, uint32_t box_n) {
-    const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N),
-                              static_cast<uint64_t>(E)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2};
-    const uint32_t box[3] = {64, box_n, 1};
-    return encode(m, base, 3, dims, strides, box);
-}
-
-// [rows, cols] bf16 seen as {64 columns, rows, cols/64 blocks}: one box {64, 64, nblk} brings
-// nblk 64-column blocks of 64 rows, each block a contiguous 8 KB in shared memory.
-bool encode_row_blocks(CUtensorMap* m, const void* base, int64_t rows, int cols, uint32_t nblk) {
+// [rows, cols] bf16 seen as {64 columns, rows, cols/64 blocks}: one box {64, box_rows, 2}
+// brings two 64-column blocks of box_rows rows, each block box_rows x 128 B, one after the
+// other in shared memory.
+bool encode_row_blocks(CUtensorMap* m, const void* base, int64_t rows, int cols, uint32_t box_rows) {
     const uint64_t dims[3] = {64, static_cast<uint64_t>(rows), static_cast<uint64_t>(cols / 64)};
     const uint64_t strides[2] = {static_cast<uint64_t>(cols) * 2, 128};
-    const uint32_t box[3] = {64, 64, nblk};
+    const uint32_t box[3] = {64, box_rows, 2};
     return encode(m, base, 3, dims, strides, box);
 }
 
-// W [E, N, K] seen as {64 k, N, K/64 blocks, E}: box {64, 64, 2, 1} brings two 64-wide k blocks
-// of 64 n-rows of one expert.
+// W [E, N, K] seen as {64 k, N, K/64 blocks, E}: box {64, 128, 2, 1} brings two 64-wide k
+// blocks of 128 n-rows of one expert (fwd: 128 n x 128 k; dgrad: 128 k x 128 n).
 bool encode_weight_blocks(CUtensorMap* m, const void* base, int E, int N, int K) {
     const uint64_t dims[4] = {64, static_cast<uint64_t>(N), static_cast<uint64_t>(K / 64),
                               static_cast<uint64_t>(E)};
     const uint64_t strides[3] = {static_cast<uint64_t>(K) * 2, 128,
                                  static_cast<uint64_t>(N) * K * 2};
-    const uint32_t box[4] = {64, 64, 2, 1};
+    const uint32_t box[4] = {64, 128, 2, 1};
     return encode(m, base, 4, dims, strides, box);
 }
 
@@ -96,17 +82,41 @@ bool encode_weight_blocks(CUtensorMap* m, const void* base, int E, int N, int K)
 struct DeviceInfo {
     std::atomic<int> ready{0};
     int sms = 0;
+    int pairs[3] = {0, 0, 0};   // co-resident CTA pairs of grouped_gemm_kernel<op>
     unsigned int* err = nullptr;
     std::mutex mu;
 };
 
 DeviceInfo g_dev[kMaxDevices];
 
+// Sets the kernel's shared-memory size and finds how many CTA pairs fit on the device at
+// once (the persistent grid).  The grid size never changes results, only speed.
 template <int OP>
-cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(gdg::grouped_gemm_kernel<OP>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(gdg::kGemmSmemBytes));
+cudaError_t set_up_kernel(int sms, int* pairs) {
+    cudaError_t e = cudaFuncSetAttribute(gdg::grouped_gemm_kernel<OP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(gdg::kGemmSmemBytes));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
+    cfg.blockDim = dim3(gdg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = gdg::kGemmSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gdg::grouped_gemm_kernel<OP>, &cfg) != cudaSuccess ||
+        n <= 0) {
+        cudaGetLastError();
+        n = sms / 2;
+    }
+    *pairs = n;
+    return cudaSuccess;
 }
 
 // Per-device set-up, once: SM count, device error word address, kernel attributes.
@@ -123,9 +133,9 @@ DeviceInfo* device_info(gdg_status* st) {
         void* err = nullptr;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaGetSymbolAddress(&err, g_device_error) != cudaSuccess ||
-            set_smem_attr<gdg::OP_FWD>() != cudaSuccess ||
-            set_smem_attr<gdg::OP_DGRAD>() != cudaSuccess ||
-            set_smem_attr<gdg::OP_WGRAD>() != cudaSuccess) {
+            set_up_kernel<gdg::OP_FWD>(d.sms, &d.pairs[0]) != cudaSuccess ||
+            set_up_kernel<gdg::OP_DGRAD>(d.sms, &d.pairs[1]) != cudaSuccess ||
+            set_up_kernel<gdg::OP_WGRAD>(d.sms, &d.pairs[2]) != cudaSuccess) {
             *st = GDG_ECUDA;
             return nullptr;
         }
@@ -153,7 +163,13 @@ Range range_of(const void* p, uint64_t bytes) {
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int tiles_per_expert(int N, int K) {
-    return (N / gdg::kBM) * static_cast<int>(ceil_div(K, gdg::kBN));
+    return (N / gdg::kPairM) * static_cast<int>(ceil_div(K, gdg::kBN));
+}
+
+// Persistent grid: two CTAs per pair, at most one pair per unit.
+int pair_grid(int64_t units, int pairs) {
+    const int64_t n = units < pairs ? units : pairs;
+    return static_cast<int>(2 * (n > 0 ? n : 1));
 }
 
 int32_t auto_split_rows(int64_t rows, int E, int N, int K) {
@@ -161,8 +177,8 @@ int32_t auto_split_rows(int64_t rows, int E, int N, int K) {
     // Shapes with few output tiles leave SMs idle in the unsplit form; cut the rows of
     // each group into fixed chunks instead.  The rule looks at shapes only, so the
     // bits never depend on the GPU it runs on.
-    if (rows <= 0 || static_cast<int64_t>(E) * tpe >= 256) return -1;
-    int64_t r = ceil_div(rows * tpe, 512);
+    if (rows <= 0 || static_cast<int64_t>(E) * tpe >= 64) return -1;
+    int64_t r = ceil_div(rows * tpe, 128);
     r = ceil_div(r, 64) * 64;
     if (r < 128) r = 128;
     if (r > (1 << 30)) r = 1 << 30;
@@ -219,11 +235,9 @@ gdg_status run_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N,
 
     GemmParams p;
     std::memset(&p, 0, sizeof p);
-    if (OP == gdg::OP_FWD ? !encode_weights(&p.tmA, args->b, E, N, K, 128u)
-                          : !encode_weight_blocks(&p.tmA, args->b, E, N, K))
-        return GDG_ECUDA;
+    if (!encode_weight_blocks(&p.tmA, args->b, E, N, K)) return GDG_ECUDA;
     for (int i = 0; i < 5; ++i)
-        if (!encode_rows(&p.tmB[i], args->a, rows, in_cols, 16u << i)) return GDG_ECUDA;
+        if (!encode_row_blocks(&p.tmB[i], args->a, rows, in_cols, 8u << i)) return GDG_ECUDA;
     p.offs = offs;
     p.out = args->out;
     p.partial = nullptr;
@@ -235,11 +249,11 @@ gdg_status run_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N,
     p.offs_kind = args->offs_kind;
     p.epi = gdg::EPI_BF16;
     p.split_rows = 0;
-    const int64_t ft = (OP == gdg::OP_FWD) ? N / gdg::kBM : ceil_div(K, gdg::kBM);
+    const int64_t ft = (OP == gdg::OP_FWD) ? N / gdg::kPairM : ceil_div(K, gdg::kPairM);
     const int64_t ub = ft * (ceil_div(rows, gdg::kRowTile) + E);
     if (ub > INT32_MAX) return GDG_EINVAL;
     p.max_units = static_cast<int>(ub);
-    const int grid = static_cast<int>(ub < dev->sms ? ub : dev->sms);
+    const int grid = pair_grid(ub, dev->pairs[OP]);
     gdg::grouped_gemm_kernel<OP><<<grid, gdg::kThreads, gdg::kGemmSmemBytes,
                                    static_cast<cudaStream_t>(stream)>>>(p);
     return launch_status(cudaGetLastError());
@@ -327,8 +341,8 @@ gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int
     const int64_t map_rows = rows > 0 ? rows : 1;
     const void* a = rows > 0 ? args->a : args->out;
     const void* b = rows > 0 ? args->b : args->out;
-    if (!encode_row_blocks(&p.tmA, a, map_rows, N, 2u) ||
-        !encode_row_blocks(&p.tmB[0], b, map_rows, K, 4u))
+    if (!encode_row_blocks(&p.tmA, a, map_rows, N, 128u) ||
+        !encode_row_blocks(&p.tmB[0], b, map_rows, K, 128u))
         return GDG_ECUDA;
     p.offs = offs;
     p.out = args->out;
@@ -343,7 +357,7 @@ gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int
     p.split_rows = split ? split_rows : 0;
     p.max_units = static_cast<int>(max_units);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int grid = static_cast<int>(max_units < dev->sms ? max_units : dev->sms);
+    const int grid = pair_grid(max_units, dev->pairs[gdg::OP_WGRAD]);
     gdg::grouped_gemm_kernel<gdg::OP_WGRAD><<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
     st = launch_status(cudaGetLastError());
     if (st != GDG_OK || !split) return st;

@@ -7,12 +7,13 @@
 //   dgrad  dX[s_e:t_e] = G[s_e:t_e] @ W[e]
 //   wgrad  dW[e]       = G[s_e:t_e]^T @ X[s_e:t_e]
 //
-// Every kernel is persistent: one CTA per SM walks work units u = blockIdx.x,
-// blockIdx.x + gridDim.x, ...  The unit list is built on the device from the offsets
-// (no host sync): each CTA reads offs, counts the units of every group and takes an
-// exclusive prefix sum in shared memory; a binary search maps u back to its group.
+// Every GEMM kernel is persistent and runs as CTA pairs (clusters of two CTAs on two SMs):
+// pair i walks work units u = i, i + pairs, ...  The unit list is built on the device from
+// the offsets (no host sync): each CTA reads offs, counts the units of every group and takes
+// an exclusive prefix sum in shared memory; a binary search maps u back to its group.
 //
-// MMA orientation (tcgen05.mma, M = 128, N <= 256, K = 16 per instruction):
+// MMA (tcgen05.mma.cta_group::2, M = 256 across the pair, N <= 256, K = 16 per instruction;
+// each CTA holds 128 rows of A, half of the N rows of B, and its 128 rows of D in TMEM):
 //   fwd    D[n, row] = sum_k  W[e][n][k] * X[row][k]   A = W  K-major,  B = X  K-major
 //   dgrad  D[k, row] = sum_n  W[e][n][k] * G[row][n]   A = W  MN-major, B = G  K-major
 //   wgrad  D[n, k]   = sum_r  G[r][n]    * X[r][k]     A = G  MN-major, B = X  MN-major
@@ -21,14 +22,16 @@
 // 128-row granularity of the M dimension; weights stream as the A operand.
 // For wgrad the reduction runs over the group's rows in 64-row stages starting exactly
 // at the group's first row; in the last stage the rows past the group end are zeroed
-// in shared memory and the MMAs past the last 16-row step are skipped.
+// in shared memory (in both CTAs) and the MMAs past the last 16-row step are skipped.
 //
-// Warp roles (256 threads): warp 0 lane 0 issues TMA loads into a kStages-deep ring;
-// warp 1 lane 0 issues tcgen05.mma into one of two TMEM accumulators (2 x 256 fp32
-// columns); warp 2 owns the TMEM allocation; warps 4..7 drain TMEM (tcgen05.ld) and
-// write the outputs while the next tile's MMAs run into the other accumulator.
+// Warp roles (256 threads per CTA): warp 0 lane 0 issues TMA loads of this CTA's halves
+// into a kStages-deep ring, completing on the even CTA's "full" barriers; warp 1 lane 0 of
+// the even CTA issues the pair's MMAs into one of two TMEM accumulators (2 x 256 fp32
+// columns) and commits to the "empty" / "tmem full" barriers of both CTAs; warp 2 owns the
+// TMEM allocation; warps 4..7 of both CTAs drain their TMEM rows (tcgen05.ld) and write the
+// outputs while the next tile's MMAs run into the other accumulator.
 //
-// Determinism: each output element is produced by exactly one CTA, whose MMA sequence
+// Determinism: each output element is produced by exactly one CTA pair, whose MMA sequence
 // is fixed by the unit's coordinates alone (never by the grid size or timing); the
 // split form writes each partial once and the reduce adds partials in chunk order.
 // No atomics touch the data.
@@ -41,20 +44,23 @@
 
 namespace gdg {
 
-constexpr int kBM = 128;                    // MMA M
+constexpr int kPairM = 256;                 // MMA M across the CTA pair
+constexpr int kBM = 128;                    // A rows (and D rows) per CTA
 constexpr int kBN = 256;                    // MMA N (max)
-constexpr int kBK = 64;                     // reduction elements per stage (128 B of bf16)
-constexpr int kStages = 4;
-constexpr int kABytes = kBM * kBK * 2;      // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;      // 32 KB
-constexpr int kBoxBytes = 64 * 128;         // one 64 x 64 bf16 TMA box
+constexpr int kBK = 128;                    // reduction elements per stage: two 64-wide blocks
+constexpr int kStages = 3;
+constexpr int kABytes = kBM * kBK * 2;      // 32 KB: this CTA's 128 rows of A
+constexpr int kBBytes = (kBN / 2) * kBK * 2;   // 32 KB: this CTA's half of B (<= 128 rows)
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kSubBytes = 128 * 128;        // one 128-row block of 64 bf16 (128 B) per row
 constexpr int kThreads = 256;
 constexpr int kMaxE = 1024;
 constexpr int kTmemCols = 512;
 constexpr int kRowTile = 256;               // fwd / dgrad: packed rows per tile
-constexpr int kPartialElems = kBM * kBN;    // fp32 elements per split partial tile
+constexpr int kPartialElems = kPairM * kBN; // fp32 elements per split partial tile
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // any single wait > 2 s is a hang
 constexpr uint64_t kDrainLimitNs = 100000000ull;
+constexpr uint64_t kPeerCopyDrainNs = 2000000ull;  // odd CTA after an abort: copies land by then
 
 enum Op : int { OP_FWD = 0, OP_DGRAD = 1, OP_WGRAD = 2 };
 enum Epi : int { EPI_BF16 = 0, EPI_FP32 = 1, EPI_BF16_ACC = 2, EPI_FP32_ACC = 3, EPI_PARTIAL = 4 };
@@ -62,13 +68,13 @@ enum Epi : int { EPI_BF16 = 0, EPI_FP32 = 1, EPI_BF16_ACC = 2, EPI_FP32_ACC = 3,
 constexpr unsigned kDevErrTimeout = 6u;
 
 struct GemmParams {
-    CUtensorMap tmA;        // fwd: W box{64,128,1}; dgrad: W {k%64, n, k/64, e} box{64,64,2,1};
-                            // wgrad: G {n%64, row, n/64} box{64,64,2}
-    CUtensorMap tmB[5];     // fwd: X, dgrad: G, box{64, 16<<i}; wgrad: tmB[0] = X
-                            // {k%64, row, k/64} box{64,64,4}
+    CUtensorMap tmA;        // fwd / dgrad: W {k%64, n, k/64, e} box{64,128,2,1};
+                            // wgrad: G {n%64, row, n/64} box{64,128,2}
+    CUtensorMap tmB[5];     // fwd: X {k%64, row, k/64}, dgrad: G {n%64, row, n/64},
+                            // box{64, 8<<i, 2}; wgrad: tmB[0] = X {k%64, row, k/64} box{64,128,2}
     const int32_t* offs;
     void* out;
-    float* partial;         // wgrad split form: [max_units][128][256] fp32
+    float* partial;         // wgrad split form: [max_units][256][256] fp32
     unsigned int* err;      // device error word
     int64_t rows;
     int E, N, K;
@@ -79,10 +85,10 @@ struct GemmParams {
 };
 
 struct SmemCtl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
+    uint64_t full[kStages];     // even CTA: both CTAs' copies of a stage have landed
+    uint64_t empty[kStages];    // both CTAs: the pair's MMAs have read the stage
+    uint64_t tfull[2];          // both CTAs: the accumulator is complete
+    uint64_t tempty[2];         // even CTA: all 8 epilogue warps of the pair drained it
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -94,21 +100,21 @@ struct SmemCtl {
 };
 
 constexpr size_t kGemmSmemBytes =
-    1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes) + sizeof(SmemCtl);
+    1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(SmemCtl);
 
 // ------------------------------------------------------------------ schedule
 
 struct Shape {
-    int ft;     // feature tiles (fwd, dgrad) or tiles per expert (wgrad)
+    int ft;     // feature tiles (fwd, dgrad) or tiles per expert (wgrad), 256 wide
     int kt;     // wgrad: k tiles per expert
 };
 
 template <int OP>
 __device__ __forceinline__ Shape unit_shape(const GemmParams& p) {
     Shape s;
-    if (OP == OP_FWD) { s.ft = p.N / kBM; s.kt = 1; }
-    else if (OP == OP_DGRAD) { s.ft = (p.K + kBM - 1) / kBM; s.kt = 1; }
-    else { s.kt = (p.K + kBN - 1) / kBN; s.ft = (p.N / kBM) * s.kt; }
+    if (OP == OP_FWD) { s.ft = p.N / kPairM; s.kt = 1; }
+    else if (OP == OP_DGRAD) { s.ft = (p.K + kPairM - 1) / kPairM; s.kt = 1; }
+    else { s.kt = (p.K + kBN - 1) / kBN; s.ft = (p.N / kPairM) * s.kt; }
     return s;
 }
 
@@ -200,7 +206,7 @@ __device__ __forceinline__ int find_group(const int* prefix, int E, int u) {
 
 struct Tile {
     int e;
-    int f0;      // first M index (fwd: n, dgrad: k, wgrad: n)
+    int f0;      // first M index of the pair tile (fwd: n, dgrad: k, wgrad: n)
     int c0;      // first N index (fwd/dgrad: packed row, wgrad: k)
     int ncols;   // valid N extent (<= 256)
     int r0;      // wgrad: first reduction row
@@ -221,7 +227,7 @@ __device__ __forceinline__ Tile decode_unit(const GemmParams& p, const SmemCtl* 
         const int sp = local / sh.ft;
         const int rem = local - sp * sh.ft;
         const int nt = rem / sh.kt, kt = rem - nt * sh.kt;
-        t.f0 = nt * kBM;
+        t.f0 = nt * kPairM;
         t.c0 = kt * kBN;
         t.ncols = min(kBN, p.K - t.c0);
         if (p.split_rows > 0) {
@@ -234,7 +240,7 @@ __device__ __forceinline__ Tile decode_unit(const GemmParams& p, const SmemCtl* 
     } else {
         const int rc_n = (m + kRowTile - 1) / kRowTile;
         const int ft = local / rc_n, rc = local - ft * rc_n;
-        t.f0 = ft * kBM;
+        t.f0 = ft * kPairM;
         t.c0 = s + rc * kRowTile;
         t.ncols = min(kRowTile, m - rc * kRowTile);
         t.r0 = 0;
@@ -244,20 +250,40 @@ __device__ __forceinline__ Tile decode_unit(const GemmParams& p, const SmemCtl* 
     return t;
 }
 
+// fwd / dgrad: MMA N (rows of the tile rounded up to 16), each CTA's half of it, and the
+// index i of the smallest row box (8 << i rows) that holds that half.
+__device__ __forceinline__ void row_split(int ncols, int& n_mma, int& half, int& bi) {
+    n_mma = (ncols + 15) & ~15;
+    half = n_mma >> 1;
+    bi = 0;
+    while ((8 << bi) < half) ++bi;
+}
+
 // ------------------------------------------------------------------ waits
 
-// Bounded wait on an mbarrier phase.  Gives up when another role has aborted, or after
-// kWaitLimitNs, in which case it raises the abort flag and records a timeout.
+struct Pair {
+    uint32_t rank;        // 0 (even CTA: issues the MMAs) or 1
+    uint32_t peer_abort;  // shared::cluster address of the other CTA's abort flag
+};
+
+__device__ __forceinline__ void raise_abort(SmemCtl* c, const Pair& pr, unsigned int* err) {
+    *reinterpret_cast<volatile int*>(&c->abort_flag) = 1;
+    st_cluster_u32(pr.peer_abort, 1u);
+    atomicCAS(err, 0u, kDevErrTimeout);
+}
+
+// Bounded wait on an mbarrier phase (cluster-scope acquire).  Gives up when either CTA of
+// the pair has aborted, or after kWaitLimitNs, in which case it raises the abort flag of
+// both CTAs and records a timeout.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SmemCtl* c,
-                                         unsigned int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
+                                         const Pair& pr, unsigned int* err) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_cluster(bar, parity)) return true;
         if (*reinterpret_cast<volatile int*>(&c->abort_flag)) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            *reinterpret_cast<volatile int*>(&c->abort_flag) = 1;
-            atomicCAS(err, 0u, kDevErrTimeout);
+            raise_abort(c, pr, err);
             return false;
         }
     }
@@ -266,12 +292,12 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SmemCtl
 // Lane 0 waits (bounded); on success the other lanes then observe the completed phase
 // themselves, which cannot move on before this warp acts, so their waits return at once.
 __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, SmemCtl* c,
-                                              unsigned int* err) {
+                                              const Pair& pr, unsigned int* err) {
     const int lane = threadIdx.x & 31;
     int ok = 1;
-    if (lane == 0) ok = wait_bar(bar, parity, c, err);
+    if (lane == 0) ok = wait_bar(bar, parity, c, pr, err);
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok && lane != 0) ok = wait_bar(bar, parity, c, err);
+    if (ok && lane != 0) ok = wait_bar(bar, parity, c, pr, err);
     return __all_sync(0xffffffffu, ok) != 0;
 }
 
@@ -279,8 +305,14 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, Sm
 // before the CTA releases its shared memory and TMEM.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_cluster(bar, parity)) {
         if (globaltimer_ns() - t0 > kDrainLimitNs) break;
+    }
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < ns) {
     }
 }
 
@@ -356,16 +388,21 @@ __device__ __forceinline__ void store_row32(int epi, void* dst_base, size_t off,
 // ------------------------------------------------------------------ the GEMM kernel
 
 template <int OP>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
+    // Same offset in both CTAs of the pair: the MMA reads A and B of both at one address.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + kStages * kABytes;
-    SmemCtl* c = reinterpret_cast<SmemCtl*>(sB + kStages * kBBytes);
+    SmemCtl* c = reinterpret_cast<SmemCtl*>(smem + kStages * kStageBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Shape sh = unit_shape<OP>(p);
+    Pair pr;
+    pr.rank = cluster_ctarank();
+    pr.peer_abort = mapa_shared(smem_u32(&c->abort_flag), pr.rank ^ 1u);
+    const bool even = pr.rank == 0;
+    const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -374,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&c->tfull[b], 1);
-            mbar_init(&c->tempty[b], 4 * 32);
+            mbar_init(&c->tempty[b], 8);   // one arrival per epilogue warp of the pair
         }
         mbar_init(&c->drain, 1);
         c->abort_flag = 0;
@@ -386,12 +423,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         else
             for (int i = 0; i < 5; ++i) prefetch_tmap(&p.tmB[i]);
     }
-    if (warp == 2) {
-        tmem_alloc(&c->tmem_base, kTmemCols);
-        tmem_relinquish();
-    }
     build_schedule<OP>(p.offs, p.offs_kind, p.rows, p.E, p.split_rows, p.max_units, sh,
                        c->start, c->size, c->prefix, c->warp_tot, &c->total);
+    // Both CTAs' barriers are initialised (and the peer has started) before any CTA signals
+    // the other's barriers or allocates TMEM together with it.
+    cluster_sync();
+    if (warp == 2) {
+        tmem_alloc_pair(&c->tmem_base, kTmemCols);
+        tmem_relinquish_pair();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -399,39 +439,45 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const int total = c->total;
 
     if (warp == 0) {
-        // ---------------------------------------------------------- TMA producer
+        // ---------------------------------------------------------- TMA producer (both CTAs)
         if (lane == 0) {
+            const uint32_t full0 = mapa_shared(smem_u32(&c->full[0]), 0u);
             int stage = 0;
             uint32_t phase = 0, filled = 0, fill_parity = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+            for (int u = pair; u < total && ok; u += npairs) {
                 const Tile t = decode_unit<OP>(p, c, sh, u);
-                int bi = 0;
-                if (OP != OP_WGRAD)
-                    while ((16 << bi) < t.ncols) ++bi;
+                int n_mma = 0, half = 0, bi = 0;
+                if (OP != OP_WGRAD) row_split(t.ncols, n_mma, half, bi);
+                const uint32_t bytes = (OP == OP_WGRAD)
+                                           ? 2u * (kABytes + kBBytes)
+                                           : 2u * (kABytes + (8u << bi) * 256u);
+                const int fa = t.f0 + kBM * static_cast<int>(pr.rank);   // this CTA's A rows
                 for (int kb = 0; kb < t.nkb; ++kb) {
-                    if (!wait_bar(&c->empty[stage], phase ^ 1u, c, p.err)) { ok = false; break; }
-                    uint8_t* a = sA + stage * kABytes;
-                    uint8_t* b = sB + stage * kBBytes;
-                    uint64_t* fb = &c->full[stage];
+                    if (!wait_bar(&c->empty[stage], phase ^ 1u, c, pr, p.err)) { ok = false; break; }
+                    uint8_t* a = smem + stage * kStageBytes;
+                    uint8_t* b = a + kABytes;
+                    const uint32_t fb = full0 + stage * 8u;
+                    if (even) mbar_arrive_expect_tx(&c->full[stage], bytes);
+                    // One copy per operand and stage: each map's third dimension walks
+                    // 64-column blocks, so two blocks land as consecutive sub-tiles (a block
+                    // past the tensor's extent reads as zeros).
                     if (OP == OP_FWD) {
-                        mbar_arrive_expect_tx(fb, kABytes + (16u << bi) * 128u);
-                        tma_load_3d(a, &p.tmA, fb, kb * kBK, t.f0, t.e);
-                        tma_load_2d(b, &p.tmB[bi], fb, kb * kBK, t.c0);
+                        // A: 128 n-rows of W[e] x k blocks 2kb, 2kb+1; B: rows x the same k.
+                        tma_load_4d_pair(a, &p.tmA, fb, 0, fa, 2 * kb, t.e);
+                        tma_load_3d_pair(b, &p.tmB[bi], fb, 0,
+                                         t.c0 + half * static_cast<int>(pr.rank), 2 * kb);
                     } else if (OP == OP_DGRAD) {
-                        // One copy brings both 64-wide k blocks of W[e] (a block past K
-                        // reads as zeros): the map's third dimension walks the blocks.
-                        mbar_arrive_expect_tx(fb, 2u * kBoxBytes + (16u << bi) * 128u);
-                        tma_load_4d(a, &p.tmA, fb, 0, kb * kBK, t.f0 / 64, t.e);
-                        tma_load_2d(b, &p.tmB[bi], fb, kb * kBK, t.c0);
+                        // A: n-rows 128kb.. of W[e] x this CTA's two 64-wide k blocks.
+                        tma_load_4d_pair(a, &p.tmA, fb, 0, kb * kBK, fa / 64, t.e);
+                        tma_load_3d_pair(b, &p.tmB[bi], fb, 0,
+                                         t.c0 + half * static_cast<int>(pr.rank), 2 * kb);
                     } else {
-                        // One copy per operand: the maps' third dimension walks 64-column
-                        // blocks, so G's two blocks and X's four land as consecutive 8 KB
-                        // boxes (blocks past K read as zeros).
+                        // 128 reduction rows x this CTA's two 64-wide blocks of G and of X.
                         const int r = t.r0 + kb * kBK;
-                        mbar_arrive_expect_tx(fb, 6u * kBoxBytes);
-                        tma_load_3d(a, &p.tmA, fb, 0, r, t.f0 / 64);
-                        tma_load_3d(b, &p.tmB[0], fb, 0, r, t.c0 / 64);
+                        tma_load_3d_pair(a, &p.tmA, fb, 0, r, fa / 64);
+                        tma_load_3d_pair(b, &p.tmB[0], fb, 0, r,
+                                         (t.c0 + (kBN / 2) * static_cast<int>(pr.rank)) / 64);
                     }
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
@@ -439,90 +485,113 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
             }
             if (!ok) {
-                // Let every copy this thread started land before the CTA exits.
-                for (int s = 0; s < kStages; ++s)
-                    if (filled & (1u << s)) drain_wait(&c->full[s], (fill_parity >> s) & 1u);
+                // Let every copy this thread started land before the CTA exits.  The even
+                // CTA sees them complete on its full barriers; the odd CTA cannot observe
+                // its copies (they complete on the even CTA's barriers) and waits a fixed
+                // time that covers any copy in flight.
+                if (even) {
+                    for (int s = 0; s < kStages; ++s)
+                        if (filled & (1u << s)) drain_wait(&c->full[s], (fill_parity >> s) & 1u);
+                } else {
+                    spin_ns(kPeerCopyDrainNs);
+                }
             }
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
-        int stage = 0, it = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++it) {
-            const Tile t = decode_unit<OP>(p, c, sh, u);
-            const int buf = it & 1;
-            if (!wait_bar_warp(&c->tempty[buf], ((it >> 1) & 1) ^ 1u, c, p.err)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kBN);
-            const uint32_t n_mma = (OP == OP_WGRAD) ? static_cast<uint32_t>(t.ncols)
-                                                    : static_cast<uint32_t>((t.ncols + 15) & ~15);
-            const uint32_t idesc = idesc_bf16(kBM, n_mma, OP != OP_FWD, OP == OP_WGRAD);
-            for (int kb = 0; kb < t.nkb; ++kb) {
-                if (!wait_bar_warp(&c->full[stage], phase, c, p.err)) { ok = false; break; }
+        // ---------------------------------------------------------- MMA issuer (even CTA)
+        if (even) {
+            const uint32_t peer_base = mapa_shared(smem_u32(smem), 1u);
+            int stage = 0, it = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int u = pair; u < total && ok; u += npairs, ++it) {
+                const Tile t = decode_unit<OP>(p, c, sh, u);
+                const int buf = it & 1;
+                if (!wait_bar_warp(&c->tempty[buf], ((it >> 1) & 1) ^ 1u, c, pr, p.err)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                uint8_t* a = sA + stage * kABytes;
-                uint8_t* b = sB + stage * kBBytes;
-                int nsteps = kBK / 16;
-                if (OP == OP_WGRAD) {
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kBN);
+                int n_mma = kBN, half = 0, bi = 0;
+                if (OP != OP_WGRAD) row_split(t.ncols, n_mma, half, bi);
+                const uint32_t idesc = idesc_bf16(kPairM, static_cast<uint32_t>(n_mma),
+                                                  OP != OP_FWD, OP == OP_WGRAD);
+                for (int kb = 0; kb < t.nkb; ++kb) {
+                    if (!wait_bar_warp(&c->full[stage], phase, c, pr, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    uint8_t* a = smem + stage * kStageBytes;
                     const int valid = t.nred - kb * kBK;
-                    if (valid < kBK) {
-                        // Last stage of this unit: rows [valid, 16 * nsteps) of every box
-                        // hold rows of another group (or another split); zero them.  A whole
-                        // 128-byte row is zeroed, so the swizzle of its 16-byte chunks does
-                        // not matter.
-                        nsteps = (valid + 15) >> 4;
-                        const int zlo = valid * 128, zhi = nsteps * 16 * 128;
-                        const int chunks = (zhi - zlo) >> 4;
-                        const int nbox = 2 + t.ncols / 64;
-                        for (int i = lane; i < nbox * chunks; i += 32) {
-                            const int bx = i / chunks, ch = i - bx * chunks;
-                            uint8_t* base = bx < 2 ? a + bx * kBoxBytes : b + (bx - 2) * kBoxBytes;
-                            *reinterpret_cast<uint4*>(base + zlo + ch * 16) = make_uint4(0, 0, 0, 0);
+                    // fwd / dgrad: a last stage of 64 (K or N is a multiple of 64) skips the
+                    // zero-filled second block.
+                    int nsteps = valid < kBK ? (valid + 15) >> 4 : kBK / 16;
+                    if (OP == OP_WGRAD) {
+                        if (valid < kBK) {
+                            // Last stage of this unit: rows [valid, 16 * nsteps) of every
+                            // sub-tile of both CTAs hold rows of another group (or another
+                            // split); zero them.  A whole 128-byte row is zeroed, so the swizzle
+                            // of its 16-byte chunks does not matter.
+                            const int zlo = valid * 128, zhi = nsteps * 16 * 128;
+                            const int chunks = (zhi - zlo) >> 4;
+                            const uint32_t off = static_cast<uint32_t>(stage * kStageBytes);
+                            for (int i = lane; i < 8 * chunks; i += 32) {
+                                const int bx = i / chunks, ch = i - bx * chunks;
+                                const uint32_t o = off + static_cast<uint32_t>((bx & 3) * kSubBytes +
+                                                                               zlo + ch * 16);
+                                if (bx < 4) *reinterpret_cast<uint4*>(smem + o) = make_uint4(0, 0, 0, 0);
+                                else st_cluster_zero16(peer_base + o);
+                            }
+                            fence_proxy_async_cluster();
+                            __syncwarp();
                         }
-                        fence_proxy_async_smem();
-                        __syncwarp();
                     }
-                }
-                if (lane == 0) {
-                    const uint32_t a_addr = smem_u32(a), b_addr = smem_u32(b);
-                    for (int kk = 0; kk < nsteps; ++kk) {
-                        const uint64_t ad = (OP == OP_FWD)
-                                                ? sdesc_sw128(a_addr + kk * 32, 16, 1024)
-                                                : sdesc_sw128(a_addr + kk * 2048, kBoxBytes, 1024);
-                        const uint64_t bd = (OP == OP_WGRAD)
-                                                ? sdesc_sw128(b_addr + kk * 2048, kBoxBytes, 1024)
-                                                : sdesc_sw128(b_addr + kk * 32, 16, 1024);
-                        umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                    if (lane == 0) {
+                        const uint32_t a_addr = smem_u32(a), b_addr = a_addr + kABytes;
+                        // K-major sub-tiles: 16-element steps are 32 B apart within a 64-wide
+                        // block, blocks are sub-tile bytes apart.  MN-major: 16 reduction rows
+                        // are 2 KB apart; the two 64-wide M/N blocks are kSubBytes apart (LBO).
+                        const uint32_t b_sub = static_cast<uint32_t>((8 << bi) * 128);
+                        for (int kk = 0; kk < nsteps; ++kk) {
+                            const uint32_t kblk = static_cast<uint32_t>(kk >> 2), k16 = kk & 3;
+                            const uint64_t ad =
+                                (OP == OP_FWD)
+                                    ? sdesc_sw128(a_addr + kblk * kSubBytes + k16 * 32, 16, 1024)
+                                    : sdesc_sw128(a_addr + kk * 2048, kSubBytes, 1024);
+                            const uint64_t bd =
+                                (OP == OP_WGRAD)
+                                    ? sdesc_sw128(b_addr + kk * 2048, kSubBytes, 1024)
+                                    : sdesc_sw128(b_addr + kblk * b_sub + k16 * 32, 16, 1024);
+                            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                        }
+                        umma_commit_pair(&c->empty[stage], 3);
                     }
-                    umma_commit(&c->empty[stage]);
+                    __syncwarp();
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
+                if (!ok) break;
+                // Arrives once this tile's MMAs (if any: an empty group has none) are done.
+                if (lane == 0) umma_commit_pair(&c->tfull[buf], 3);
                 __syncwarp();
-                if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
-            if (!ok) break;
+            // Every MMA this thread issued has completed once this commit arrives.
             if (lane == 0) {
-                if (t.nkb > 0) umma_commit(&c->tfull[buf]);
-                else mbar_arrive(&c->tfull[buf]);   // empty group: nothing to wait for
+                umma_commit_pair(&c->drain, 1);
+                drain_wait(&c->drain, 0);
             }
             __syncwarp();
         }
-        // Every MMA this thread issued has completed once this commit arrives.
-        if (lane == 0) {
-            umma_commit(&c->drain);
-            drain_wait(&c->drain, 0);
-        }
-        __syncwarp();
     } else if (warp >= 4) {
-        // ---------------------------------------------------------- epilogue
+        // ---------------------------------------------------------- epilogue (both CTAs)
         const int q = warp & 3;                 // TMEM lanes [32q, 32q + 32)
+        const int mrow = kBM * static_cast<int>(pr.rank) + q * 32 + lane;   // row of the pair tile
+        const uint32_t tempty0 = mapa_shared(smem_u32(&c->tempty[0]), 0u);
         int it = 0;
-        for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+        for (int u = pair; u < total; u += npairs, ++it) {
             const Tile t = decode_unit<OP>(p, c, sh, u);
             const int buf = it & 1;
-            if (!wait_bar_warp(&c->tfull[buf], (it >> 1) & 1, c, p.err)) break;
+            if (!wait_bar_warp(&c->tfull[buf], (it >> 1) & 1, c, pr, p.err)) break;
             tc_fence_after();
-            const int f = t.f0 + q * 32 + lane;
+            const int f = t.f0 + mrow;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(buf * kBN);
             const int nchunks = (t.ncols + 31) >> 5;
@@ -537,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
                 if (OP == OP_WGRAD) {
                     if (p.epi == EPI_PARTIAL) {
-                        const size_t off = (static_cast<size_t>(t.u) * kBM + q * 32 + lane) * kBN + ch * 32;
+                        const size_t off = (static_cast<size_t>(t.u) * kPairM + mrow) * kBN + ch * 32;
                         store_row32(EPI_FP32, p.partial, off, r);
                     } else {
                         const size_t off = (static_cast<size_t>(t.e) * p.N + f) * p.K + t.c0 + ch * 32;
@@ -557,15 +626,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
             }
             tc_fence_before();
-            mbar_arrive(&c->tempty[buf]);
+            __syncwarp();
+            if (lane == 0) {
+                if (even) mbar_arrive(&c->tempty[buf]);
+                else mbar_arrive_cluster(tempty0 + buf * 8u);
+            }
         }
     }
 
+    // Neither CTA leaves (or frees TMEM) while the other may still signal its barriers or
+    // read its shared memory.
     tc_fence_before();
     __syncthreads();
+    __syncwarp();
+    cluster_sync();
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc_pair(tmem_base, kTmemCols);
     }
 }
 
@@ -597,7 +674,7 @@ __global__ void __launch_bounds__(kThreads) wgrad_reduce_kernel(const __grid_con
     __shared__ ReduceSmem sm;
     Shape sh;
     sh.kt = (p.K + kBN - 1) / kBN;
-    sh.ft = (p.N / kBM) * sh.kt;
+    sh.ft = (p.N / kPairM) * sh.kt;
     build_schedule<OP_WGRAD>(p.offs, p.offs_kind, p.rows, p.E, p.split_rows, p.max_units, sh,
                              sm.start, sm.size, sm.prefix, sm.warp_tot, &sm.total);
     const int64_t NK = static_cast<int64_t>(p.N) * p.K;
@@ -610,8 +687,8 @@ __global__ void __launch_bounds__(kThreads) wgrad_reduce_kernel(const __grid_con
         const int n = static_cast<int>(rem / p.K);
         const int k = static_cast<int>(rem - static_cast<int64_t>(n) * p.K);
         const int S = (sm.size[e] + p.split_rows - 1) / p.split_rows;
-        const int tile = (n / kBM) * sh.kt + k / kBN;
-        const size_t within = static_cast<size_t>(n % kBM) * kBN + (k % kBN);
+        const int tile = (n / kPairM) * sh.kt + k / kBN;
+        const size_t within = static_cast<size_t>(n % kPairM) * kBN + (k % kBN);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s = 0; s < S; ++s) {
             const int u = sm.prefix[e] + s * sh.ft + tile;

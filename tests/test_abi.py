@@ -109,9 +109,9 @@ def test_workspace_bytes_and_auto_form(lib):
     g.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     assert f(0, 512, 4, 256, 256, 0, 0, 0) == 0 and f(1, 512, 4, 256, 256, 0, 0, 0) == 0
     assert f(2, 512, 4, 256, 256, 1, 0, -1) == 0
-    # split rows 64 on [E=4, N=256, K=256]: (N/128)*(K/256) = 2 tiles per expert,
-    # at most ceil(512/64) + 4 = 12 chunks -> 24 partial tiles of 128 x 256 fp32
-    assert f(2, 512, 4, 256, 256, 1, 1, 64) == 24 * 128 * 256 * 4
+    # split rows 64 on [E=4, N=256, K=256]: (N/256)*(K/256) = 1 tile per expert,
+    # at most ceil(512/64) + 4 = 12 chunks -> 12 partial tiles of 256 x 256 fp32
+    assert f(2, 512, 4, 256, 256, 1, 1, 64) == 12 * 256 * 256 * 4
     assert f(2, 512, 4, 256, 256, 0, 0, 100) == ctypes.c_size_t(-1).value
     assert f(3, 512, 4, 256, 256, 0, 0, 0) == ctypes.c_size_t(-1).value
     # the automatic form depends on shapes only
