@@ -38,9 +38,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// bf16 tensor map with 128-byte swizzle; OOB elements read as zero.
-bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-            const uint64_t* strides_bytes, const uint32_t* box) {
+// Tensor map; OOB elements read as zero.
+bool encode_map(CUtensorMap* m, CUtensorMapDataType type, CUtensorMapSwizzle swz,
+                const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                const uint32_t* box) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t d[4];
@@ -49,11 +50,28 @@ bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
     cuuint32_t es[4] = {1, 1, 1, 1};
     for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
     for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
-                    const_cast<void*>(base), d, s, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    CUresult r = fn(m, type, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// bf16 operand map with 128-byte swizzle (the MMA's shared-memory layout).
+bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+            const uint64_t* strides_bytes, const uint32_t* box) {
+    return encode_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, base, rank,
+                      dims, strides_bytes, box);
+}
+
+// wgrad output [rows, cols] (bf16 or fp32) for the epilogue's 32-row staging boxes of 64 B
+// (64-byte swizzle), or, with prefetch = true, for L2 prefetches of 128 x 256 blocks.
+bool encode_out(CUtensorMap* m, void* base, int64_t rows, int cols, bool fp32, bool prefetch) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(cols) * (fp32 ? 4u : 2u)};
+    const uint32_t box[2] = {prefetch ? 256u : (fp32 ? 16u : 32u), prefetch ? 128u : 32u};
+    return encode_map(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      prefetch ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B, base, 2,
+                      dims, strides, box);
 }
 
 // [rows, cols] bf16 seen as {64 columns, rows, cols/64 blocks}: one box {64, box_rows, 2}
@@ -199,6 +217,7 @@ gdg_status check_common(const gdg_args* args, const int32_t* offs, int E, int N,
     if (out_dtype != GDG_BF16 && out_dtype != GDG_FP32) return GDG_EINVAL;
     if (N % 256 != 0 || K % 64 != 0) return GDG_EALIGN;
     if (static_cast<int64_t>(E) * N * K > (int64_t{1} << 40)) return GDG_EINVAL;
+    if (static_cast<int64_t>(E) * N >= INT32_MAX) return GDG_EINVAL;   // TMA row coordinates
     if (!offs) return GDG_EINVAL;
     (void)offs;
     return GDG_OK;
@@ -328,7 +347,7 @@ gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int
             (rows > 0 && (overlaps(r_w, r_a) || overlaps(r_w, r_b))))
             return GDG_EOVERLAP;
     }
-    if (max_units > INT32_MAX) return GDG_EINVAL;
+    if (max_units * gdg::kPairM >= INT32_MAX) return GDG_EINVAL;   // TMA row coordinates
 
     DeviceInfo* dev = device_info(&st);
     if (!dev) return st;
@@ -344,6 +363,16 @@ gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int
     if (!encode_row_blocks(&p.tmA, a, map_rows, N, 128u) ||
         !encode_row_blocks(&p.tmB[0], b, map_rows, K, 128u))
         return GDG_ECUDA;
+    if (split) {
+        if (!encode_out(&p.tmOut, args->workspace, max_units * gdg::kPairM, gdg::kBN, true, false))
+            return GDG_ECUDA;
+    } else {
+        const bool f32 = out_dtype == GDG_FP32;
+        if (!encode_out(&p.tmOut, args->out, static_cast<int64_t>(E) * N, K, f32, false) ||
+            (accumulate &&
+             !encode_out(&p.tmPre, args->out, static_cast<int64_t>(E) * N, K, f32, true)))
+            return GDG_ECUDA;
+    }
     p.offs = offs;
     p.out = args->out;
     p.partial = split ? static_cast<float*>(args->workspace) : nullptr;
@@ -375,9 +404,9 @@ gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int
     r.split_rows = split_rows;
     r.max_units = static_cast<int>(max_units);
     const int64_t vec4 = static_cast<int64_t>(E) * N * K / 4;
-    int64_t rgrid = ceil_div(vec4, gdg::kThreads);
+    int64_t rgrid = ceil_div(vec4, gdg::kReduceThreads);
     if (rgrid > static_cast<int64_t>(dev->sms) * 8) rgrid = static_cast<int64_t>(dev->sms) * 8;
-    gdg::wgrad_reduce_kernel<<<static_cast<int>(rgrid), gdg::kThreads, 0, s>>>(r);
+    gdg::wgrad_reduce_kernel<<<static_cast<int>(rgrid), gdg::kReduceThreads, 0, s>>>(r);
     return launch_status(cudaGetLastError());
 }
 

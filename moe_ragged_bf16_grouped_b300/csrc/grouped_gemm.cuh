@@ -8,9 +8,9 @@
 //   wgrad  dW[e]       = G[s_e:t_e]^T @ X[s_e:t_e]
 //
 // Every GEMM kernel is persistent and runs as CTA pairs (clusters of two CTAs on two SMs):
-// pair i walks work units u = i, i + pairs, ...  The unit list is built on the device from
-// the offsets (no host sync): each CTA reads offs, counts the units of every group and takes
-// an exclusive prefix sum in shared memory; a binary search maps u back to its group.
+// pair i walks work units u = i, i + pairs, ...  The unit list comes from the offsets on the
+// device (no host sync): units are numbered group by group, each CTA counts them once, and
+// every role keeps a cursor that walks the groups forward (reading offs) as u grows.
 //
 // MMA (tcgen05.mma.cta_group::2, M = 256 across the pair, N <= 256, K = 16 per instruction;
 // each CTA holds 128 rows of A, half of the N rows of B, and its 128 rows of D in TMEM):
@@ -20,16 +20,19 @@
 // For fwd / dgrad the packed rows are the MMA's N dimension, so a ragged group is
 // covered with 16-row granularity (N = round_up(rows in tile, 16)) instead of the
 // 128-row granularity of the M dimension; weights stream as the A operand.
-// For wgrad the reduction runs over the group's rows in 64-row stages starting exactly
-// at the group's first row; in the last stage the rows past the group end are zeroed
-// in shared memory (in both CTAs) and the MMAs past the last 16-row step are skipped.
+// For wgrad the reduction runs over the group's rows in 128-row stages starting exactly
+// at the group's first row.  A unit's last stage usually runs past the group end: its
+// copies complete on a barrier of their own CTA, a "fixer" warp in each CTA zeroes the
+// rows past the end in its own shared memory, and the two fixers' arrivals release the
+// stage to the MMA, which skips the steps past the last 16-row step.
 //
 // Warp roles (256 threads per CTA): warp 0 lane 0 issues TMA loads of this CTA's halves
 // into a kStages-deep ring, completing on the even CTA's "full" barriers; warp 1 lane 0 of
 // the even CTA issues the pair's MMAs into one of two TMEM accumulators (2 x 256 fp32
 // columns) and commits to the "empty" / "tmem full" barriers of both CTAs; warp 2 owns the
-// TMEM allocation; warps 4..7 of both CTAs drain their TMEM rows (tcgen05.ld) and write the
-// outputs while the next tile's MMAs run into the other accumulator.
+// TMEM allocation; warp 3 of each CTA zeroes wgrad tail rows; warps 4..11 of both CTAs drain
+// their TMEM rows (tcgen05.ld; two warps per 32-lane quarter, one per half of the columns)
+// and write the outputs while the next tile's MMAs run into the other accumulator.
 //
 // Determinism: each output element is produced by exactly one CTA pair, whose MMA sequence
 // is fixed by the unit's coordinates alone (never by the grid size or timing); the
@@ -53,14 +56,20 @@ constexpr int kABytes = kBM * kBK * 2;      // 32 KB: this CTA's 128 rows of A
 constexpr int kBBytes = (kBN / 2) * kBK * 2;   // 32 KB: this CTA's half of B (<= 128 rows)
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kSubBytes = 128 * 128;        // one 128-row block of 64 bf16 (128 B) per row
-constexpr int kThreads = 256;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiBufs = 2;                 // wgrad: staging boxes per epilogue warp
+constexpr int kEpiBoxBytes = 32 * 64;       // one staging box: 32 rows x 64 B, 64-byte swizzle
+constexpr int kEpiBytes = kEpiWarps * kEpiBufs * kEpiBoxBytes;
+constexpr int kThreads = 384;               // GEMM kernel: 4 role warps + 8 epilogue warps
+constexpr int kReduceThreads = 256;
 constexpr int kMaxE = 1024;
 constexpr int kTmemCols = 512;
 constexpr int kRowTile = 256;               // fwd / dgrad: packed rows per tile
 constexpr int kPartialElems = kPairM * kBN; // fp32 elements per split partial tile
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // any single wait > 2 s is a hang
 constexpr uint64_t kDrainLimitNs = 100000000ull;
-constexpr uint64_t kPeerCopyDrainNs = 2000000ull;  // odd CTA after an abort: copies land by then
+constexpr uint32_t kSuspendNs = 20000;             // sleep hint of a waiting thread
+constexpr uint64_t kCopyDrainNs = 2000000ull;   // after an abort: copies in flight land by then
 
 enum Op : int { OP_FWD = 0, OP_DGRAD = 1, OP_WGRAD = 2 };
 enum Epi : int { EPI_BF16 = 0, EPI_FP32 = 1, EPI_BF16_ACC = 2, EPI_FP32_ACC = 3, EPI_PARTIAL = 4 };
@@ -72,6 +81,9 @@ struct GemmParams {
                             // wgrad: G {n%64, row, n/64} box{64,128,2}
     CUtensorMap tmB[5];     // fwd: X {k%64, row, k/64}, dgrad: G {n%64, row, n/64},
                             // box{64, 8<<i, 2}; wgrad: tmB[0] = X {k%64, row, k/64} box{64,128,2}
+    CUtensorMap tmOut;      // wgrad: dW as {K, E*N} (split: partials as {256, units*256}),
+                            // box {32 bf16 | 16 fp32, 32 rows}, 64-byte swizzle
+    CUtensorMap tmPre;      // wgrad accumulate: dW as {K, E*N}, box {256, 128}, no swizzle
     const int32_t* offs;
     void* out;
     float* partial;         // wgrad split form: [max_units][256][256] fp32
@@ -85,22 +97,22 @@ struct GemmParams {
 };
 
 struct SmemCtl {
-    uint64_t full[kStages];     // even CTA: both CTAs' copies of a stage have landed
+    uint64_t full[kStages];     // even CTA: both CTAs' copies of a stage have landed (a wgrad
+                                // tail stage: both CTAs' fixers have zeroed its tail rows)
     uint64_t empty[kStages];    // both CTAs: the pair's MMAs have read the stage
+    uint64_t tail_full[kStages];   // both CTAs (wgrad): this CTA's copies of a tail stage
+    uint64_t epi_full[kEpiWarps][kEpiBufs];   // wgrad accumulate: an old-value box has landed
     uint64_t tfull[2];          // both CTAs: the accumulator is complete
-    uint64_t tempty[2];         // even CTA: all 8 epilogue warps of the pair drained it
+    uint64_t tempty[2];         // even CTA: all 16 epilogue warps of the pair drained it
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
     int total;
     int warp_tot[kThreads / 32];
-    int start[kMaxE];
-    int size[kMaxE];
-    int prefix[kMaxE + 1];
 };
 
 constexpr size_t kGemmSmemBytes =
-    1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(SmemCtl);
+    1024 + static_cast<size_t>(kStages) * kStageBytes + kEpiBytes + sizeof(SmemCtl);
 
 // ------------------------------------------------------------------ schedule
 
@@ -122,8 +134,8 @@ __device__ __forceinline__ Shape unit_shape(const GemmParams& p) {
 __device__ __forceinline__ void group_range(const int32_t* offs, int kind, int64_t rows, int e,
                                             int& s, int& m) {
     int64_t a, b;
-    if (kind == 0) { a = e > 0 ? offs[e - 1] : 0; b = offs[e]; }
-    else { a = offs[e]; b = offs[e + 1]; }
+    if (kind == 0) { a = e > 0 ? __ldg(offs + e - 1) : 0; b = __ldg(offs + e); }
+    else { a = __ldg(offs + e); b = __ldg(offs + e + 1); }
     a = a < 0 ? 0 : (a > rows ? rows : a);
     b = b < 0 ? 0 : (b > rows ? rows : b);
     if (b < a) b = a;
@@ -140,7 +152,8 @@ __device__ __forceinline__ int units_of_group(int m, const Shape& sh, int split_
     return ((m + kRowTile - 1) / kRowTile) * sh.ft;
 }
 
-// Builds start/size/prefix/total in shared memory.  Every thread of the block calls it.
+// Builds start/size/prefix/total in shared memory (ordered reduce of split partials).  Every
+// thread of the block (kReduceThreads) calls it.
 template <int OP>
 __device__ void build_schedule(const int32_t* offs, int kind, int64_t rows, int E,
                                int split_rows, int max_units, const Shape& sh, int* start,
@@ -169,13 +182,13 @@ __device__ void build_schedule(const int32_t* offs, int kind, int64_t rows, int 
     if (lane == 31) warp_tot[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int t = lane < kThreads / 32 ? warp_tot[lane] : 0;
+        int t = lane < kReduceThreads / 32 ? warp_tot[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, t, o);
             if (lane >= o) t += y;
         }
-        if (lane < kThreads / 32) warp_tot[lane] = t;
+        if (lane < kReduceThreads / 32) warp_tot[lane] = t;
     }
     __syncthreads();
     int base = (warp ? warp_tot[warp - 1] : 0) + x - local;
@@ -186,23 +199,64 @@ __device__ void build_schedule(const int32_t* offs, int kind, int64_t rows, int 
         base += v[j];
     }
     if (tid == 0) {
-        const int tot = warp_tot[kThreads / 32 - 1];
+        const int tot = warp_tot[kReduceThreads / 32 - 1];
         prefix[E] = tot;
         *total = tot < max_units ? tot : max_units;
     }
     __syncthreads();
 }
 
-// Largest e with prefix[e] <= u (prefix[0] == 0, non-decreasing).
-__device__ __forceinline__ int find_group(const int* prefix, int E, int u) {
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (prefix[mid] <= u) lo = mid;
-        else hi = mid - 1;
+// Number of work units over all groups, capped at max_units.  Every thread of the block
+// calls it.
+template <int OP>
+__device__ int count_units(const GemmParams& p, const Shape& sh, int* warp_tot) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int local = 0;
+    for (int e = tid; e < p.E; e += kThreads) {
+        int s, m;
+        group_range(p.offs, p.offs_kind, p.rows, e, s, m);
+        local += units_of_group<OP>(m, sh, p.split_rows);
     }
-    return lo;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+    if (lane == 0) warp_tot[warp] = local;
+    __syncthreads();
+    int tot = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) tot += warp_tot[w];
+    return tot < p.max_units ? tot : p.max_units;
 }
+
+// Walks the groups forward: group e holds units [base, base + n) and rows [s, s + m).
+struct Cursor {
+    int e, base, n, s, m;
+};
+
+template <int OP>
+__device__ __forceinline__ void cursor_init(Cursor& cu, const GemmParams& p, const Shape& sh) {
+    cu.e = 0;
+    cu.base = 0;
+    group_range(p.offs, p.offs_kind, p.rows, 0, cu.s, cu.m);
+    cu.n = units_of_group<OP>(cu.m, sh, p.split_rows);
+}
+
+// Moves the cursor to the group that holds unit u (u never decreases between calls, and
+// u < total, so the last group is never passed).
+template <int OP>
+__device__ __forceinline__ void cursor_seek(Cursor& cu, const GemmParams& p, const Shape& sh,
+                                            int u) {
+    while (u >= cu.base + cu.n && cu.e + 1 < p.E) {
+        cu.base += cu.n;
+        ++cu.e;
+        group_range(p.offs, p.offs_kind, p.rows, cu.e, cu.s, cu.m);
+        cu.n = units_of_group<OP>(cu.m, sh, p.split_rows);
+    }
+}
+
+// wgrad: a stage whose rows end inside a 16-row MMA step (rows of another group or split
+// follow in that step) must have those rows zeroed before the MMAs read it.
+__device__ __forceinline__ bool needs_fix(int valid) { return valid < kBK && (valid & 15) != 0; }
+
 
 struct Tile {
     int e;
@@ -216,13 +270,14 @@ struct Tile {
 };
 
 template <int OP>
-__device__ __forceinline__ Tile decode_unit(const GemmParams& p, const SmemCtl* c,
-                                            const Shape& sh, int u) {
+__device__ __forceinline__ Tile decode_unit(const GemmParams& p, Cursor& cu, const Shape& sh,
+                                            int u) {
+    cursor_seek<OP>(cu, p, sh, u);
     Tile t;
     t.u = u;
-    t.e = find_group(c->prefix, p.E, u);
-    const int local = u - c->prefix[t.e];
-    const int s = c->start[t.e], m = c->size[t.e];
+    t.e = cu.e;
+    const int local = u - cu.base;
+    const int s = cu.s, m = cu.m;
     if (OP == OP_WGRAD) {
         const int sp = local / sh.ft;
         const int rem = local - sp * sh.ft;
@@ -280,7 +335,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SmemCtl
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (mbar_try_wait_cluster(bar, parity, kSuspendNs)) return true;
         if (*reinterpret_cast<volatile int*>(&c->abort_flag)) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             raise_abort(c, pr, err);
@@ -326,65 +381,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// Writes 32 consecutive fp32 accumulator values of one dW row with the chosen epilogue.
-//   EPI_BF16     : dW = bf16_rn(acc)
-//   EPI_FP32     : dW = acc
-//   EPI_BF16_ACC : out = bf16_rn(float(out) + float(bf16_rn(acc)))   (bf16 out.add_(dW))
-//   EPI_FP32_ACC : out = out + acc, one fp32 RN add                   (fp32 out.add_(dW))
-//   EPI_PARTIAL  : fp32 partial tile row
-__device__ __forceinline__ void store_row32(int epi, void* dst_base, size_t off,
-                                            const uint32_t (&r)[32]) {
-    if (epi == EPI_BF16) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dst_base) + off);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
-            v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
-            v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
-            v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
-            dst[q] = v;
-        }
-    } else if (epi == EPI_BF16_ACC) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dst_base) + off);
-        uint4 old[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) old[q] = dst[q];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint32_t o[4] = {old[q].x, old[q].y, old[q].z, old[q].w};
-            uint32_t nv[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const uint32_t d = pack_bf16x2(__uint_as_float(r[8 * q + 2 * h]),
-                                               __uint_as_float(r[8 * q + 2 * h + 1]));
-                nv[h] = pack_bf16x2(__fadd_rn(bf16_lo(o[h]), bf16_lo(d)),
-                                    __fadd_rn(bf16_hi(o[h]), bf16_hi(d)));
-            }
-            dst[q] = make_uint4(nv[0], nv[1], nv[2], nv[3]);
-        }
-    } else {
-        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(dst_base) + off);
-        if (epi == EPI_FP32_ACC) {
-            float4 old[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) old[q] = dst[q];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                dst[q] = make_float4(__fadd_rn(old[q].x, __uint_as_float(r[4 * q + 0])),
-                                     __fadd_rn(old[q].y, __uint_as_float(r[4 * q + 1])),
-                                     __fadd_rn(old[q].z, __uint_as_float(r[4 * q + 2])),
-                                     __fadd_rn(old[q].w, __uint_as_float(r[4 * q + 3])));
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                dst[q] = make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
-                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-        }
-    }
-}
-
 // ------------------------------------------------------------------ the GEMM kernel
 
 template <int OP>
@@ -394,7 +390,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Same offset in both CTAs of the pair: the MMA reads A and B of both at one address.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    SmemCtl* c = reinterpret_cast<SmemCtl*>(smem + kStages * kStageBytes);
+    uint8_t* stage_area = smem + kStages * kStageBytes;      // wgrad epilogue staging boxes
+    SmemCtl* c = reinterpret_cast<SmemCtl*>(stage_area + kEpiBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Shape sh = unit_shape<OP>(p);
@@ -406,25 +403,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&c->full[s], 1);
+            // wgrad: a stage is released by two arrivals, the even producer's two (plain
+            // stage) or one per CTA's fixer (tail stage).
+            mbar_init(&c->full[s], OP == OP_WGRAD ? 2 : 1);
             mbar_init(&c->empty[s], 1);
+            mbar_init(&c->tail_full[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&c->tfull[b], 1);
-            mbar_init(&c->tempty[b], 8);   // one arrival per epilogue warp of the pair
+            mbar_init(&c->tempty[b], 2 * kEpiWarps);   // one arrival per epilogue warp of the pair
         }
+        for (int w = 0; w < kEpiWarps; ++w)
+            for (int b = 0; b < kEpiBufs; ++b) mbar_init(&c->epi_full[w][b], 1);
         mbar_init(&c->drain, 1);
         c->abort_flag = 0;
         fence_mbar_init();
     }
     if (tid == 32) {
         prefetch_tmap(&p.tmA);
-        if (OP == OP_WGRAD) prefetch_tmap(&p.tmB[0]);
-        else
+        if (OP == OP_WGRAD) {
+            prefetch_tmap(&p.tmB[0]);
+            prefetch_tmap(&p.tmOut);
+        } else
             for (int i = 0; i < 5; ++i) prefetch_tmap(&p.tmB[i]);
     }
-    build_schedule<OP>(p.offs, p.offs_kind, p.rows, p.E, p.split_rows, p.max_units, sh,
-                       c->start, c->size, c->prefix, c->warp_tot, &c->total);
+    const int total = count_units<OP>(p, sh, c->warp_tot);
+    Cursor cu;
+    cursor_init<OP>(cu, p, sh);
     // Both CTAs' barriers are initialised (and the peer has started) before any CTA signals
     // the other's barriers or allocates TMEM together with it.
     cluster_sync();
@@ -436,29 +441,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = c->tmem_base;
-    const int total = c->total;
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer (both CTAs)
         if (lane == 0) {
             const uint32_t full0 = mapa_shared(smem_u32(&c->full[0]), 0u);
+            const uint32_t tail0 = mapa_shared(smem_u32(&c->tail_full[0]), pr.rank);
             int stage = 0;
-            uint32_t phase = 0, filled = 0, fill_parity = 0;
+            uint32_t phase = 0;
             bool ok = true;
             for (int u = pair; u < total && ok; u += npairs) {
-                const Tile t = decode_unit<OP>(p, c, sh, u);
+                const Tile t = decode_unit<OP>(p, cu, sh, u);
                 int n_mma = 0, half = 0, bi = 0;
                 if (OP != OP_WGRAD) row_split(t.ncols, n_mma, half, bi);
                 const uint32_t bytes = (OP == OP_WGRAD)
                                            ? 2u * (kABytes + kBBytes)
                                            : 2u * (kABytes + (8u << bi) * 256u);
                 const int fa = t.f0 + kBM * static_cast<int>(pr.rank);   // this CTA's A rows
+                if (OP == OP_WGRAD && (p.epi == EPI_FP32_ACC || p.epi == EPI_BF16_ACC))
+                    // The epilogue reads this CTA's 128 x 256 block of out after the unit's
+                    // mainloop: start bringing it into L2 now.
+                    tma_prefetch_2d(&p.tmPre, t.c0, t.e * p.N + fa);
                 for (int kb = 0; kb < t.nkb; ++kb) {
                     if (!wait_bar(&c->empty[stage], phase ^ 1u, c, pr, p.err)) { ok = false; break; }
                     uint8_t* a = smem + stage * kStageBytes;
                     uint8_t* b = a + kABytes;
-                    const uint32_t fb = full0 + stage * 8u;
-                    if (even) mbar_arrive_expect_tx(&c->full[stage], bytes);
+                    uint32_t fb = full0 + stage * 8u;
+                    if (OP == OP_WGRAD && needs_fix(t.nred - kb * kBK)) {
+                        // Tail stage: this CTA's copies complete on its own barrier; its fixer
+                        // zeroes the rows past the group end, then releases the stage.
+                        fb = tail0 + stage * 8u;
+                        mbar_arrive_expect_tx(&c->tail_full[stage], kABytes + kBBytes);
+                    } else if (even) {
+                        mbar_arrive_expect_tx(&c->full[stage], bytes);
+                        if (OP == OP_WGRAD) mbar_arrive(&c->full[stage]);
+                    }
                     // One copy per operand and stage: each map's third dimension walks
                     // 64-column blocks, so two blocks land as consecutive sub-tiles (a block
                     // past the tensor's extent reads as zeros).
@@ -479,33 +496,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         tma_load_3d_pair(b, &p.tmB[0], fb, 0, r,
                                          (t.c0 + (kBN / 2) * static_cast<int>(pr.rank)) / 64);
                     }
-                    filled |= 1u << stage;
-                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
             }
-            if (!ok) {
-                // Let every copy this thread started land before the CTA exits.  The even
-                // CTA sees them complete on its full barriers; the odd CTA cannot observe
-                // its copies (they complete on the even CTA's barriers) and waits a fixed
-                // time that covers any copy in flight.
-                if (even) {
-                    for (int s = 0; s < kStages; ++s)
-                        if (filled & (1u << s)) drain_wait(&c->full[s], (fill_parity >> s) & 1u);
-                } else {
-                    spin_ns(kPeerCopyDrainNs);
-                }
-            }
+            // After an abort, let every copy this thread started land before the CTA exits.
+            // Most complete on the even CTA's barriers, which this CTA cannot observe, so it
+            // waits a fixed time that covers any copy in flight.
+            if (!ok) spin_ns(kCopyDrainNs);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer (even CTA)
         if (even) {
-            const uint32_t peer_base = mapa_shared(smem_u32(smem), 1u);
             int stage = 0, it = 0;
             uint32_t phase = 0;
             bool ok = true;
             for (int u = pair; u < total && ok; u += npairs, ++it) {
-                const Tile t = decode_unit<OP>(p, c, sh, u);
+                const Tile t = decode_unit<OP>(p, cu, sh, u);
                 const int buf = it & 1;
                 if (!wait_bar_warp(&c->tempty[buf], ((it >> 1) & 1) ^ 1u, c, pr, p.err)) {
                     ok = false;
@@ -525,26 +531,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // fwd / dgrad: a last stage of 64 (K or N is a multiple of 64) skips the
                     // zero-filled second block.
                     int nsteps = valid < kBK ? (valid + 15) >> 4 : kBK / 16;
-                    if (OP == OP_WGRAD) {
-                        if (valid < kBK) {
-                            // Last stage of this unit: rows [valid, 16 * nsteps) of every
-                            // sub-tile of both CTAs hold rows of another group (or another
-                            // split); zero them.  A whole 128-byte row is zeroed, so the swizzle
-                            // of its 16-byte chunks does not matter.
-                            const int zlo = valid * 128, zhi = nsteps * 16 * 128;
-                            const int chunks = (zhi - zlo) >> 4;
-                            const uint32_t off = static_cast<uint32_t>(stage * kStageBytes);
-                            for (int i = lane; i < 8 * chunks; i += 32) {
-                                const int bx = i / chunks, ch = i - bx * chunks;
-                                const uint32_t o = off + static_cast<uint32_t>((bx & 3) * kSubBytes +
-                                                                               zlo + ch * 16);
-                                if (bx < 4) *reinterpret_cast<uint4*>(smem + o) = make_uint4(0, 0, 0, 0);
-                                else st_cluster_zero16(peer_base + o);
-                            }
-                            fence_proxy_async_cluster();
-                            __syncwarp();
-                        }
-                    }
                     if (lane == 0) {
                         const uint32_t a_addr = smem_u32(a), b_addr = a_addr + kABytes;
                         // K-major sub-tiles: 16-element steps are 32 B apart within a 64-wide
@@ -580,22 +566,198 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         }
+    } else if (warp == 3) {
+        // ---------------------------------------------------------- wgrad tail fixer (both CTAs)
+        if (OP == OP_WGRAD) {
+            const uint32_t full0 = mapa_shared(smem_u32(&c->full[0]), 0u);
+            int stage = 0;
+            uint32_t tphase = 0;     // per stage: parity of the next tail_full phase
+            bool ok = true;
+            for (int u = pair; u < total && ok; u += npairs) {
+                const Tile t = decode_unit<OP>(p, cu, sh, u);
+                for (int kb = 0; kb < t.nkb; ++kb) {
+                    const int valid = t.nred - kb * kBK;
+                    if (needs_fix(valid)) {
+                        if (!wait_bar_warp(&c->tail_full[stage], (tphase >> stage) & 1u, c, pr,
+                                           p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tphase ^= 1u << stage;
+                        // Rows [valid, round_up(valid, 16)) of this CTA's four sub-tiles (A and
+                        // B, two 64-wide blocks each) hold rows of another group or another
+                        // split: zero them.  A whole 128-byte row is zeroed, so the swizzle of
+                        // its 16-byte chunks does not matter.
+                        const int zlo = valid * 128, zhi = ((valid + 15) & ~15) * 128;
+                        const int chunks = (zhi - zlo) >> 4;
+                        uint8_t* base = smem + stage * kStageBytes;
+                        for (int i = lane; i < 4 * chunks; i += 32) {
+                            const int bx = i / chunks, ch = i - bx * chunks;
+                            *reinterpret_cast<uint4*>(base + bx * kSubBytes + zlo + ch * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (even) mbar_arrive(&c->full[stage]);
+                            else mbar_arrive_cluster(full0 + stage * 8u);
+                        }
+                        __syncwarp();
+                    }
+                    if (++stage == kStages) stage = 0;
+                }
+            }
+        }
+    } else if (warp >= 4 && OP == OP_WGRAD) {
+        // ---------------------------------------------------------- wgrad epilogue (both CTAs)
+        // Each warp drains its 32 TMEM lanes (32 dW rows) 32 columns at a time, converts,
+        // writes 32-row x 64-byte boxes into shared memory in the 64-byte swizzle pattern and
+        // stores each box with one TMA copy (whole lines to HBM).  With accumulate, the
+        // box's old values are first loaded by TMA into the same buffer (one box ahead, after
+        // an L2 prefetch of the whole block issued when the unit started).
+        const int q = warp & 3, ew = warp - 4;          // TMEM lanes [32q, 32q + 32)
+        const int hc = ew >> 2;                         // columns [128 hc, 128 hc + 128)
+        const int mrow0 = kBM * static_cast<int>(pr.rank) + q * 32;   // first row of the pair tile
+        const uint32_t tempty0 = mapa_shared(smem_u32(&c->tempty[0]), 0u);
+        uint8_t* stg = stage_area + ew * (kEpiBufs * kEpiBoxBytes);
+        const bool acc = p.epi == EPI_FP32_ACC || p.epi == EPI_BF16_ACC;
+        const bool f32 = p.epi == EPI_FP32 || p.epi == EPI_FP32_ACC || p.epi == EPI_PARTIAL;
+        const int bpc = f32 ? 2 : 1;            // boxes per 32-column chunk
+        const int box_cols = f32 ? 16 : 32;
+        // This lane's row of a staging box; 16-byte granule g sits at slot g ^ ((row >> 1) & 3).
+        const int rsw = (lane >> 1) & 3;
+        uint32_t jg = 0;         // boxes this warp has stored so far (buffer rotation)
+        uint32_t lphase = 0;     // per buffer: parity of its next load completion
+        bool ok = true;
+        int it = 0;
+        for (int u = pair; u < total; u += npairs, ++it) {
+            const Tile t = decode_unit<OP>(p, cu, sh, u);
+            const int buf = it & 1;
+            if (!wait_bar_warp(&c->tfull[buf], (it >> 1) & 1, c, pr, p.err)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(buf * kBN);
+            const int y = (p.epi == EPI_PARTIAL) ? t.u * kPairM + mrow0 : t.e * p.N + t.f0 + mrow0;
+            const int x0 = (p.epi == EPI_PARTIAL) ? 0 : t.c0;
+            const int ch0 = 4 * hc, ch1 = min(4 * hc + 4, t.ncols >> 5);
+            const int nbox = ch1 > ch0 ? (ch1 - ch0) * bpc : 0;
+            if (acc && nbox > 0 && lane == 0) {
+                // First box's old values; its buffer was last read by the store of box jg - 2.
+                bulk_wait_group_read<kEpiBufs - 1>();
+                const uint32_t b = jg % kEpiBufs;
+                mbar_arrive_expect_tx(&c->epi_full[ew][b], kEpiBoxBytes);
+                tma_load_2d(stg + b * kEpiBoxBytes, &p.tmOut, &c->epi_full[ew][b], x0 + ch0 * 32, y);
+            }
+            uint32_t r[32];
+            for (int ch = ch0; ch < ch1 && ok; ++ch) {
+                if (t.nkb > 0) {
+                    tmem_ld_32x32b_x32(taddr + ch * 32, r);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = 0u;   // +0.0f: empty group
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (h >= bpc) break;
+                    const int i = (ch - ch0) * bpc + h;
+                    const uint32_t b = (jg + i) % kEpiBufs;
+                    uint8_t* sb = stg + b * kEpiBoxBytes + lane * 64;
+                    if (acc) {
+                        if (i + 1 < nbox && lane == 0) {
+                            // Next box's old values into the other buffer, once the last store
+                            // (which read that buffer) has read it.
+                            bulk_wait_group_read<0>();
+                            const uint32_t nb = (jg + i + 1) % kEpiBufs;
+                            const int ni = i + 1, nch = ch0 + ni / bpc, nh = ni % bpc;
+                            mbar_arrive_expect_tx(&c->epi_full[ew][nb], kEpiBoxBytes);
+                            tma_load_2d(stg + nb * kEpiBoxBytes, &p.tmOut, &c->epi_full[ew][nb],
+                                        x0 + nch * 32 + nh * box_cols, y);
+                        }
+                        if (!wait_bar_warp(&c->epi_full[ew][b], (lphase >> b) & 1u, c, pr, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        lphase ^= 1u << b;
+                    } else if (jg + i >= kEpiBufs) {
+                        if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        uint4* slot = reinterpret_cast<uint4*>(sb + ((g ^ rsw) << 4));
+                        if (!f32) {
+                            const uint32_t* v = r + 8 * g;
+                            uint4 d = make_uint4(
+                                pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                                pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                                pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                                pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
+                            if (acc) {
+                                // out = bf16(float(out) + float(bf16(dW))): bf16 out.add_(dW)
+                                const uint4 o = *slot;
+                                d.x = pack_bf16x2(__fadd_rn(bf16_lo(o.x), bf16_lo(d.x)),
+                                                  __fadd_rn(bf16_hi(o.x), bf16_hi(d.x)));
+                                d.y = pack_bf16x2(__fadd_rn(bf16_lo(o.y), bf16_lo(d.y)),
+                                                  __fadd_rn(bf16_hi(o.y), bf16_hi(d.y)));
+                                d.z = pack_bf16x2(__fadd_rn(bf16_lo(o.z), bf16_lo(d.z)),
+                                                  __fadd_rn(bf16_hi(o.z), bf16_hi(d.z)));
+                                d.w = pack_bf16x2(__fadd_rn(bf16_lo(o.w), bf16_lo(d.w)),
+                                                  __fadd_rn(bf16_hi(o.w), bf16_hi(d.w)));
+                            }
+                            *slot = d;
+                        } else {
+                            const uint32_t* v = r + 16 * h + 4 * g;
+                            float4 d = make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]),
+                                                   __uint_as_float(v[2]), __uint_as_float(v[3]));
+                            if (acc) {
+                                // out = RN32(out + dW): fp32 out.add_(dW)
+                                const float4 o = *reinterpret_cast<const float4*>(slot);
+                                d = make_float4(__fadd_rn(o.x, d.x), __fadd_rn(o.y, d.y),
+                                                __fadd_rn(o.z, d.z), __fadd_rn(o.w, d.w));
+                            }
+                            *reinterpret_cast<float4*>(slot) = d;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tmOut, stg + b * kEpiBoxBytes, x0 + ch * 32 + h * box_cols, y);
+                        bulk_commit_group();
+                    }
+                }
+            }
+            if (!ok) break;
+            jg += static_cast<uint32_t>(nbox);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (even) mbar_arrive(&c->tempty[buf]);
+                else mbar_arrive_cluster(tempty0 + buf * 8u);
+            }
+        }
+        // Every store has read its box and written HBM before the CTA leaves; after an abort,
+        // an old-value load may still be in flight: give it time to land.
+        if (lane == 0) bulk_wait_group<0>();
+        if (!ok && acc) spin_ns(kCopyDrainNs);
+        __syncwarp();
     } else if (warp >= 4) {
-        // ---------------------------------------------------------- epilogue (both CTAs)
+        // ---------------------------------------------------------- fwd / dgrad epilogue
         const int q = warp & 3;                 // TMEM lanes [32q, 32q + 32)
+        const int hc = (warp - 4) >> 2;         // columns [128 hc, 128 hc + 128)
         const int mrow = kBM * static_cast<int>(pr.rank) + q * 32 + lane;   // row of the pair tile
         const uint32_t tempty0 = mapa_shared(smem_u32(&c->tempty[0]), 0u);
         int it = 0;
         for (int u = pair; u < total; u += npairs, ++it) {
-            const Tile t = decode_unit<OP>(p, c, sh, u);
+            const Tile t = decode_unit<OP>(p, cu, sh, u);
             const int buf = it & 1;
             if (!wait_bar_warp(&c->tfull[buf], (it >> 1) & 1, c, pr, p.err)) break;
             tc_fence_after();
             const int f = t.f0 + mrow;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(buf * kBN);
-            const int nchunks = (t.ncols + 31) >> 5;
-            for (int ch = 0; ch < nchunks; ++ch) {
+            const int nchunks = min((t.ncols + 31) >> 5, 4 * hc + 4);
+            for (int ch = 4 * hc; ch < nchunks; ++ch) {
                 uint32_t r[32];
                 if (t.nkb > 0) {
                     tmem_ld_32x32b_x32(taddr + ch * 32, r);
@@ -604,25 +766,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = 0u;   // +0.0f
                 }
-                if (OP == OP_WGRAD) {
-                    if (p.epi == EPI_PARTIAL) {
-                        const size_t off = (static_cast<size_t>(t.u) * kPairM + mrow) * kBN + ch * 32;
-                        store_row32(EPI_FP32, p.partial, off, r);
-                    } else {
-                        const size_t off = (static_cast<size_t>(t.e) * p.N + f) * p.K + t.c0 + ch * 32;
-                        store_row32(p.epi, p.out, off, r);
-                    }
-                } else {
-                    const int fdim = (OP == OP_FWD) ? p.N : p.K;
-                    if (f < fdim) {
-                        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-                        const int jn = min(32, t.ncols - ch * 32);
-                        const int64_t row = t.c0 + ch * 32;
+                const int fdim = (OP == OP_FWD) ? p.N : p.K;
+                if (f < fdim) {
+                    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+                    const int jn = min(32, t.ncols - ch * 32);
+                    const int64_t row = t.c0 + ch * 32;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < jn)
-                                out[(row + j) * fdim + f] = __float2bfloat16_rn(__uint_as_float(r[j]));
-                    }
+                    for (int j = 0; j < 32; ++j)
+                        if (j < jn)
+                            out[(row + j) * fdim + f] = __float2bfloat16_rn(__uint_as_float(r[j]));
                 }
             }
             tc_fence_before();
@@ -661,7 +813,7 @@ struct ReduceParams {
 };
 
 struct ReduceSmem {
-    int warp_tot[kThreads / 32];
+    int warp_tot[kReduceThreads / 32];
     int total;
     int start[kMaxE];
     int size[kMaxE];
@@ -670,7 +822,7 @@ struct ReduceSmem {
 
 // dW[e][n][k] = p_0 + p_1 + ... + p_{S_e - 1} (fp32, left to right; +0.0 when S_e = 0),
 // then the same epilogue as the unsplit kernel.  4 consecutive k per thread.
-__global__ void __launch_bounds__(kThreads) wgrad_reduce_kernel(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(kReduceThreads) wgrad_reduce_kernel(const __grid_constant__ ReduceParams p) {
     __shared__ ReduceSmem sm;
     Shape sh;
     sh.kt = (p.K + kBN - 1) / kBN;
@@ -679,8 +831,8 @@ __global__ void __launch_bounds__(kThreads) wgrad_reduce_kernel(const __grid_con
                              sm.start, sm.size, sm.prefix, sm.warp_tot, &sm.total);
     const int64_t NK = static_cast<int64_t>(p.N) * p.K;
     const int64_t total4 = static_cast<int64_t>(p.E) * NK / 4;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total4;
-         i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kReduceThreads + threadIdx.x; i < total4;
+         i += static_cast<int64_t>(gridDim.x) * kReduceThreads) {
         const int64_t idx = i * 4;
         const int e = static_cast<int>(idx / NK);
         const int64_t rem = idx - e * NK;
