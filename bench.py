@@ -336,17 +336,19 @@ def run_ours(args, world, rank, local):
     means = {k: float(np.mean(v)) for k, v in per.items()}
     dom = max(means, key=lambda k: means[k] * len(per[k]))
     achieved = flops[dom] / (means[dom] * 1e-3) / 1e12
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # Each kernel is timed inside a long back-to-back step loop (power-capped clocks), so the
+    # denominator is the sustained bf16 GEMM throughput; the burst fraction is reported too.
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     roofline = {"bound": "tensor", "kernel": KERNEL_NAMES[dom], "achieved": achieved,
                 "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": recorded_traffic(KERNEL_NAMES[dom]),
-                "peak_source": f"{peak_src}, burst bf16 (kernel timed alone in its events)",
+                "peak_source": f"{peak_src}, sustained bf16 (kernel timed inside a long step loop)",
                 "per_kernel_ms": {k: round(v, 4) for k, v in means.items()},
                 "per_kernel_tflops": {k: round(flops[k] / (means[k] * 1e-3) / 1e12, 1)
                                       for k in means},
-                "step_frac_of_nominal_2250": round(step_f / (ms_per_step * 1e-3) / 1e12 / 2250.0, 4),
-                "frac_of_sustained": round(achieved / float(peaks.get(
-                    "bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])), 4)}
+                "frac_of_burst": round(achieved / burst, 4),
+                "step_frac_of_nominal_2250": round(step_f / (ms_per_step * 1e-3) / 1e12 / 2250.0, 4)}
 
     out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
