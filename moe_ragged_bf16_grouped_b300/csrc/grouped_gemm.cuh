@@ -588,14 +588,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         // B, two 64-wide blocks each) hold rows of another group or another
                         // split: zero them.  A whole 128-byte row is zeroed, so the swizzle of
                         // its 16-byte chunks does not matter.
-                        const int zlo = valid * 128, zhi = ((valid + 15) & ~15) * 128;
-                        const int chunks = (zhi - zlo) >> 4;
-                        uint8_t* base = smem + stage * kStageBytes;
-                        for (int i = lane; i < 4 * chunks; i += 32) {
-                            const int bx = i / chunks, ch = i - bx * chunks;
-                            *reinterpret_cast<uint4*>(base + bx * kSubBytes + zlo + ch * 16) =
-                                make_uint4(0, 0, 0, 0);
-                        }
+                        // Lane l zeroes 16-byte chunk l % 8 of rows valid + l / 8, +4, ...
+                        const int zend = (valid + 15) & ~15;
+                        uint8_t* base = smem + stage * kStageBytes + (lane & 7) * 16;
+#pragma unroll
+                        for (int bx = 0; bx < 4; ++bx)
+                            for (int r = valid + (lane >> 3); r < zend; r += 4)
+                                *reinterpret_cast<uint4*>(base + bx * kSubBytes + r * 128) =
+                                    make_uint4(0, 0, 0, 0);
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
