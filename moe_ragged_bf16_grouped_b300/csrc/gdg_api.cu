@@ -63,15 +63,13 @@ bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                       dims, strides_bytes, box);
 }
 
-// wgrad output [rows, cols] (bf16 or fp32) for the epilogue's 32-row staging boxes of 64 B
-// (64-byte swizzle), or, with prefetch = true, for L2 prefetches of 128 x 256 blocks.
-bool encode_out(CUtensorMap* m, void* base, int64_t rows, int cols, bool fp32, bool prefetch) {
+// wgrad accumulate: out [rows, cols] (bf16 or fp32) for L2 prefetches of 128 x 256 blocks.
+bool encode_prefetch(CUtensorMap* m, void* base, int64_t rows, int cols, bool fp32) {
     const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
     const uint64_t strides[1] = {static_cast<uint64_t>(cols) * (fp32 ? 4u : 2u)};
-    const uint32_t box[2] = {prefetch ? 256u : (fp32 ? 16u : 32u), prefetch ? 128u : 32u};
+    const uint32_t box[2] = {256u, 128u};
     return encode_map(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      prefetch ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B, base, 2,
-                      dims, strides, box);
+                      CU_TENSOR_MAP_SWIZZLE_NONE, base, 2, dims, strides, box);
 }
 
 // [rows, cols] bf16 seen as {64 columns, rows, cols/64 blocks}: one box {64, box_rows, 2}
@@ -100,7 +98,7 @@ bool encode_weight_blocks(CUtensorMap* m, const void* base, int E, int N, int K)
 struct DeviceInfo {
     std::atomic<int> ready{0};
     int sms = 0;
-    int pairs[3] = {0, 0, 0};   // co-resident CTA pairs of grouped_gemm_kernel<op>
+    int pairs = 0;              // co-resident CTA pairs of grouped_gemm_kernel
     unsigned int* err = nullptr;
     std::mutex mu;
 };
@@ -109,9 +107,9 @@ DeviceInfo g_dev[kMaxDevices];
 
 // Sets the kernel's shared-memory size and finds how many CTA pairs fit on the device at
 // once (the persistent grid).  The grid size never changes results, only speed.
-template <int OP>
+template <int OP, int EPI>
 cudaError_t set_up_kernel(int sms, int* pairs) {
-    cudaError_t e = cudaFuncSetAttribute(gdg::grouped_gemm_kernel<OP>,
+    cudaError_t e = cudaFuncSetAttribute(gdg::grouped_gemm_kernel<OP, EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(gdg::kGemmSmemBytes));
     if (e != cudaSuccess) return e;
@@ -128,7 +126,7 @@ cudaError_t set_up_kernel(int sms, int* pairs) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gdg::grouped_gemm_kernel<OP>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&n, gdg::grouped_gemm_kernel<OP, EPI>, &cfg) != cudaSuccess ||
         n <= 0) {
         cudaGetLastError();
         n = sms / 2;
@@ -151,9 +149,13 @@ DeviceInfo* device_info(gdg_status* st) {
         void* err = nullptr;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaGetSymbolAddress(&err, g_device_error) != cudaSuccess ||
-            set_up_kernel<gdg::OP_FWD>(d.sms, &d.pairs[0]) != cudaSuccess ||
-            set_up_kernel<gdg::OP_DGRAD>(d.sms, &d.pairs[1]) != cudaSuccess ||
-            set_up_kernel<gdg::OP_WGRAD>(d.sms, &d.pairs[2]) != cudaSuccess) {
+            set_up_kernel<gdg::OP_FWD, gdg::EPI_BF16>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_DGRAD, gdg::EPI_BF16>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_BF16>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_FP32>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_BF16_ACC>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_FP32_ACC>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_PARTIAL>(d.sms, &d.pairs) != cudaSuccess) {
             *st = GDG_ECUDA;
             return nullptr;
         }
@@ -266,14 +268,13 @@ gdg_status run_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N,
     p.N = N;
     p.K = K;
     p.offs_kind = args->offs_kind;
-    p.epi = gdg::EPI_BF16;
     p.split_rows = 0;
     const int64_t ft = (OP == gdg::OP_FWD) ? N / gdg::kPairM : ceil_div(K, gdg::kPairM);
     const int64_t ub = ft * (ceil_div(rows, gdg::kRowTile) + E);
     if (ub > INT32_MAX) return GDG_EINVAL;
     p.max_units = static_cast<int>(ub);
-    const int grid = pair_grid(ub, dev->pairs[OP]);
-    gdg::grouped_gemm_kernel<OP><<<grid, gdg::kThreads, gdg::kGemmSmemBytes,
+    const int grid = pair_grid(ub, dev->pairs);
+    gdg::grouped_gemm_kernel<OP, gdg::EPI_BF16><<<grid, gdg::kThreads, gdg::kGemmSmemBytes,
                                    static_cast<cudaStream_t>(stream)>>>(p);
     return launch_status(cudaGetLastError());
 }
@@ -363,16 +364,10 @@ gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int
     if (!encode_row_blocks(&p.tmA, a, map_rows, N, 128u) ||
         !encode_row_blocks(&p.tmB[0], b, map_rows, K, 128u))
         return GDG_ECUDA;
-    if (split) {
-        if (!encode_out(&p.tmOut, args->workspace, max_units * gdg::kPairM, gdg::kBN, true, false))
-            return GDG_ECUDA;
-    } else {
-        const bool f32 = out_dtype == GDG_FP32;
-        if (!encode_out(&p.tmOut, args->out, static_cast<int64_t>(E) * N, K, f32, false) ||
-            (accumulate &&
-             !encode_out(&p.tmPre, args->out, static_cast<int64_t>(E) * N, K, f32, true)))
-            return GDG_ECUDA;
-    }
+    if (!split && accumulate &&
+        !encode_prefetch(&p.tmPre, args->out, static_cast<int64_t>(E) * N, K,
+                         out_dtype == GDG_FP32))
+        return GDG_ECUDA;
     p.offs = offs;
     p.out = args->out;
     p.partial = split ? static_cast<float*>(args->workspace) : nullptr;
@@ -382,12 +377,33 @@ gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int
     p.N = N;
     p.K = K;
     p.offs_kind = args->offs_kind;
-    p.epi = split ? gdg::EPI_PARTIAL : epi;
     p.split_rows = split ? split_rows : 0;
     p.max_units = static_cast<int>(max_units);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int grid = pair_grid(max_units, dev->pairs[gdg::OP_WGRAD]);
-    gdg::grouped_gemm_kernel<gdg::OP_WGRAD><<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+    const int grid = pair_grid(max_units, dev->pairs);
+    const int kepi = split ? static_cast<int>(gdg::EPI_PARTIAL) : epi;
+    switch (kepi) {
+        case gdg::EPI_BF16:
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_BF16>
+                <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+            break;
+        case gdg::EPI_FP32:
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_FP32>
+                <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+            break;
+        case gdg::EPI_BF16_ACC:
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_BF16_ACC>
+                <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+            break;
+        case gdg::EPI_FP32_ACC:
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_FP32_ACC>
+                <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+            break;
+        default:
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_PARTIAL>
+                <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+            break;
+    }
     st = launch_status(cudaGetLastError());
     if (st != GDG_OK || !split) return st;
 

@@ -57,9 +57,8 @@ constexpr int kBBytes = (kBN / 2) * kBK * 2;   // 32 KB: this CTA's half of B (<
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kSubBytes = 128 * 128;        // one 128-row block of 64 bf16 (128 B) per row
 constexpr int kEpiWarps = 8;
-constexpr int kEpiBufs = 2;                 // wgrad: staging boxes per epilogue warp
-constexpr int kEpiBoxBytes = 32 * 64;       // one staging box: 32 rows x 64 B, 64-byte swizzle
-constexpr int kEpiBytes = kEpiWarps * kEpiBufs * kEpiBoxBytes;
+constexpr int kEpiBoxBytes = 32 * 128;      // wgrad staging box per warp: 32 rows x 128 B
+constexpr int kEpiBytes = kEpiWarps * kEpiBoxBytes;
 constexpr int kThreads = 384;               // GEMM kernel: 4 role warps + 8 epilogue warps
 constexpr int kReduceThreads = 256;
 constexpr int kMaxE = 1024;
@@ -81,9 +80,7 @@ struct GemmParams {
                             // wgrad: G {n%64, row, n/64} box{64,128,2}
     CUtensorMap tmB[5];     // fwd: X {k%64, row, k/64}, dgrad: G {n%64, row, n/64},
                             // box{64, 8<<i, 2}; wgrad: tmB[0] = X {k%64, row, k/64} box{64,128,2}
-    CUtensorMap tmOut;      // wgrad: dW as {K, E*N} (split: partials as {256, units*256}),
-                            // box {32 bf16 | 16 fp32, 32 rows}, 64-byte swizzle
-    CUtensorMap tmPre;      // wgrad accumulate: dW as {K, E*N}, box {256, 128}, no swizzle
+    CUtensorMap tmPre;      // wgrad accumulate: out as {K, E*N}, box {256, 128} (L2 prefetch)
     const int32_t* offs;
     void* out;
     float* partial;         // wgrad split form: [max_units][256][256] fp32
@@ -91,7 +88,6 @@ struct GemmParams {
     int64_t rows;
     int E, N, K;
     int offs_kind;
-    int epi;
     int split_rows;         // wgrad: > 0 selects the split form
     int max_units;          // units at or past this index are skipped
 };
@@ -101,7 +97,6 @@ struct SmemCtl {
                                 // tail stage: both CTAs' fixers have zeroed its tail rows)
     uint64_t empty[kStages];    // both CTAs: the pair's MMAs have read the stage
     uint64_t tail_full[kStages];   // both CTAs (wgrad): this CTA's copies of a tail stage
-    uint64_t epi_full[kEpiWarps][kEpiBufs];   // wgrad accumulate: an old-value box has landed
     uint64_t tfull[2];          // both CTAs: the accumulator is complete
     uint64_t tempty[2];         // even CTA: all 16 epilogue warps of the pair drained it
     uint64_t drain;
@@ -383,7 +378,8 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 
 // ------------------------------------------------------------------ the GEMM kernel
 
-template <int OP>
+// EPI: the epilogue (fwd / dgrad: EPI_BF16; wgrad: any, EPI_PARTIAL for the split form).
+template <int OP, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -413,8 +409,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(&c->tfull[b], 1);
             mbar_init(&c->tempty[b], 2 * kEpiWarps);   // one arrival per epilogue warp of the pair
         }
-        for (int w = 0; w < kEpiWarps; ++w)
-            for (int b = 0; b < kEpiBufs; ++b) mbar_init(&c->epi_full[w][b], 1);
         mbar_init(&c->drain, 1);
         c->abort_flag = 0;
         fence_mbar_init();
@@ -423,7 +417,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         prefetch_tmap(&p.tmA);
         if (OP == OP_WGRAD) {
             prefetch_tmap(&p.tmB[0]);
-            prefetch_tmap(&p.tmOut);
         } else
             for (int i = 0; i < 5; ++i) prefetch_tmap(&p.tmB[i]);
     }
@@ -458,7 +451,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                            ? 2u * (kABytes + kBBytes)
                                            : 2u * (kABytes + (8u << bi) * 256u);
                 const int fa = t.f0 + kBM * static_cast<int>(pr.rank);   // this CTA's A rows
-                if (OP == OP_WGRAD && (p.epi == EPI_FP32_ACC || p.epi == EPI_BF16_ACC))
+                if (OP == OP_WGRAD && (EPI == EPI_FP32_ACC || EPI == EPI_BF16_ACC))
                     // The epilogue reads this CTA's 128 x 256 block of out after the unit's
                     // mainloop: start bringing it into L2 now.
                     tma_prefetch_2d(&p.tmPre, t.c0, t.e * p.N + fa);
@@ -610,24 +603,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 4 && OP == OP_WGRAD) {
         // ---------------------------------------------------------- wgrad epilogue (both CTAs)
-        // Each warp drains its 32 TMEM lanes (32 dW rows) 32 columns at a time, converts,
-        // writes 32-row x 64-byte boxes into shared memory in the 64-byte swizzle pattern and
-        // stores each box with one TMA copy (whole lines to HBM).  With accumulate, the
-        // box's old values are first loaded by TMA into the same buffer (one box ahead, after
-        // an L2 prefetch of the whole block issued when the unit started).
+        // Each warp writes 32 dW rows (its TMEM lanes) x 128 columns (one half of the tile) in
+        // boxes of 32 rows x 128 bytes (64 bf16 or 32 fp32 columns): TMEM -> registers (one
+        // row per thread) -> shared memory (128-byte swizzle) -> registers in line order (8
+        // threads per 128-byte line) -> coalesced global stores.  With accumulate the old
+        // values are loaded in the same line order (after an L2 prefetch of the block issued
+        // when the unit's loads started) and added there.
         const int q = warp & 3, ew = warp - 4;          // TMEM lanes [32q, 32q + 32)
         const int hc = ew >> 2;                         // columns [128 hc, 128 hc + 128)
         const int mrow0 = kBM * static_cast<int>(pr.rank) + q * 32;   // first row of the pair tile
         const uint32_t tempty0 = mapa_shared(smem_u32(&c->tempty[0]), 0u);
-        uint8_t* stg = stage_area + ew * (kEpiBufs * kEpiBoxBytes);
-        const bool acc = p.epi == EPI_FP32_ACC || p.epi == EPI_BF16_ACC;
-        const bool f32 = p.epi == EPI_FP32 || p.epi == EPI_FP32_ACC || p.epi == EPI_PARTIAL;
-        const int bpc = f32 ? 2 : 1;            // boxes per 32-column chunk
-        const int box_cols = f32 ? 16 : 32;
-        // This lane's row of a staging box; 16-byte granule g sits at slot g ^ ((row >> 1) & 3).
-        const int rsw = (lane >> 1) & 3;
-        uint32_t jg = 0;         // boxes this warp has stored so far (buffer rotation)
-        uint32_t lphase = 0;     // per buffer: parity of its next load completion
+        uint8_t* box = stage_area + ew * kEpiBoxBytes;
+        constexpr bool acc = EPI == EPI_FP32_ACC || EPI == EPI_BF16_ACC;
+        constexpr bool f32 = EPI == EPI_FP32 || EPI == EPI_FP32_ACC || EPI == EPI_PARTIAL;
+        constexpr int osz = f32 ? 4 : 2;
+        constexpr int box_cols = f32 ? 32 : 64;
+        const int rr = lane >> 3, gg = lane & 7;        // line-order phase: rows rr + 4j, chunk gg
+        uint8_t* wslot = box + lane * 128;              // this lane's row in the write phase
+        const int wsw = lane & 7;
         bool ok = true;
         int it = 0;
         for (int u = pair; u < total; u += npairs, ++it) {
@@ -637,98 +630,84 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(buf * kBN);
-            const int y = (p.epi == EPI_PARTIAL) ? t.u * kPairM + mrow0 : t.e * p.N + t.f0 + mrow0;
-            const int x0 = (p.epi == EPI_PARTIAL) ? 0 : t.c0;
-            const int ch0 = 4 * hc, ch1 = min(4 * hc + 4, t.ncols >> 5);
-            const int nbox = ch1 > ch0 ? (ch1 - ch0) * bpc : 0;
-            if (acc && nbox > 0 && lane == 0) {
-                // First box's old values; its buffer was last read by the store of box jg - 2.
-                bulk_wait_group_read<kEpiBufs - 1>();
-                const uint32_t b = jg % kEpiBufs;
-                mbar_arrive_expect_tx(&c->epi_full[ew][b], kEpiBoxBytes);
-                tma_load_2d(stg + b * kEpiBoxBytes, &p.tmOut, &c->epi_full[ew][b], x0 + ch0 * 32, y);
+            uint8_t* obase;
+            size_t ldo;
+            if (EPI == EPI_PARTIAL) {
+                obase = reinterpret_cast<uint8_t*>(p.partial) +
+                        (static_cast<size_t>(t.u) * kPairM + mrow0) * kBN * 4;
+                ldo = static_cast<size_t>(kBN) * 4;
+            } else {
+                ldo = static_cast<size_t>(p.K) * osz;
+                obase = reinterpret_cast<uint8_t*>(p.out) +
+                        (static_cast<size_t>(t.e) * p.N + t.f0 + mrow0) * ldo +
+                        static_cast<size_t>(t.c0) * osz;
             }
-            uint32_t r[32];
-            for (int ch = ch0; ch < ch1 && ok; ++ch) {
-                if (t.nkb > 0) {
-                    tmem_ld_32x32b_x32(taddr + ch * 32, r);
-                    tmem_ld_wait();
+            const int cend = min(128 * hc + 128, t.ncols);
+            for (int cb = 128 * hc; cb < cend; cb += box_cols) {
+                uint8_t* gline = obase + static_cast<size_t>(rr) * ldo + cb * osz + gg * 16;
+                uint4 old[8];
+                if constexpr (acc) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        old[j] = *reinterpret_cast<const uint4*>(gline + 4 * j * ldo);
+                }
+                // The box's row for this thread as 8 chunks of 16 bytes (32 words).
+                uint32_t pk[32];
+                if constexpr (f32) {
+                    if (t.nkb > 0) {
+                        tmem_ld_32x32b_x32(taddr + cb, pk);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) pk[j] = 0u;   // +0.0f: empty group
+                    }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = 0u;   // +0.0f: empty group
-                }
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (h >= bpc) break;
-                    const int i = (ch - ch0) * bpc + h;
-                    const uint32_t b = (jg + i) % kEpiBufs;
-                    uint8_t* sb = stg + b * kEpiBoxBytes + lane * 64;
-                    if (acc) {
-                        if (i + 1 < nbox && lane == 0) {
-                            // Next box's old values into the other buffer, once the last store
-                            // (which read that buffer) has read it.
-                            bulk_wait_group_read<0>();
-                            const uint32_t nb = (jg + i + 1) % kEpiBufs;
-                            const int ni = i + 1, nch = ch0 + ni / bpc, nh = ni % bpc;
-                            mbar_arrive_expect_tx(&c->epi_full[ew][nb], kEpiBoxBytes);
-                            tma_load_2d(stg + nb * kEpiBoxBytes, &p.tmOut, &c->epi_full[ew][nb],
-                                        x0 + nch * 32 + nh * box_cols, y);
-                        }
-                        if (!wait_bar_warp(&c->epi_full[ew][b], (lphase >> b) & 1u, c, pr, p.err)) {
-                            ok = false;
-                            break;
-                        }
-                        lphase ^= 1u << b;
-                    } else if (jg + i >= kEpiBufs) {
-                        if (lane == 0) bulk_wait_group_read<kEpiBufs - 1>();
-                        __syncwarp();
-                    }
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        uint4* slot = reinterpret_cast<uint4*>(sb + ((g ^ rsw) << 4));
-                        if (!f32) {
-                            const uint32_t* v = r + 8 * g;
-                            uint4 d = make_uint4(
-                                pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
-                                pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
-                                pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
-                                pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
-                            if (acc) {
-                                // out = bf16(float(out) + float(bf16(dW))): bf16 out.add_(dW)
-                                const uint4 o = *slot;
-                                d.x = pack_bf16x2(__fadd_rn(bf16_lo(o.x), bf16_lo(d.x)),
-                                                  __fadd_rn(bf16_hi(o.x), bf16_hi(d.x)));
-                                d.y = pack_bf16x2(__fadd_rn(bf16_lo(o.y), bf16_lo(d.y)),
-                                                  __fadd_rn(bf16_hi(o.y), bf16_hi(d.y)));
-                                d.z = pack_bf16x2(__fadd_rn(bf16_lo(o.z), bf16_lo(d.z)),
-                                                  __fadd_rn(bf16_hi(o.z), bf16_hi(d.z)));
-                                d.w = pack_bf16x2(__fadd_rn(bf16_lo(o.w), bf16_lo(d.w)),
-                                                  __fadd_rn(bf16_hi(o.w), bf16_hi(d.w)));
-                            }
-                            *slot = d;
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t r[32];
+                        if (t.nkb > 0) {
+                            tmem_ld_32x32b_x32(taddr + cb + 32 * h, r);
+                            tmem_ld_wait();
                         } else {
-                            const uint32_t* v = r + 16 * h + 4 * g;
-                            float4 d = make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]),
-                                                   __uint_as_float(v[2]), __uint_as_float(v[3]));
-                            if (acc) {
-                                // out = RN32(out + dW): fp32 out.add_(dW)
-                                const float4 o = *reinterpret_cast<const float4*>(slot);
-                                d = make_float4(__fadd_rn(o.x, d.x), __fadd_rn(o.y, d.y),
-                                                __fadd_rn(o.z, d.z), __fadd_rn(o.w, d.w));
-                            }
-                            *reinterpret_cast<float4*>(slot) = d;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) r[j] = 0u;
                         }
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&p.tmOut, stg + b * kEpiBoxBytes, x0 + ch * 32 + h * box_cols, y);
-                        bulk_commit_group();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            pk[16 * h + j] = pack_bf16x2(__uint_as_float(r[2 * j]),
+                                                         __uint_as_float(r[2 * j + 1]));
                     }
                 }
+                // One row per thread: 16-byte chunk g of row `lane` goes to slot g ^ (lane & 7).
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    *reinterpret_cast<uint4*>(wslot + ((g ^ wsw) << 4)) =
+                        make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int row = rr + 4 * j;
+                    uint4 v = *reinterpret_cast<const uint4*>(box + row * 128 + ((gg ^ (row & 7)) << 4));
+                    if constexpr (acc) {
+                        const uint4 o = old[j];
+                        if constexpr (f32) {
+                            // out = RN32(out + dW): fp32 out.add_(dW)
+                            v = make_uint4(__float_as_uint(__fadd_rn(__uint_as_float(o.x), __uint_as_float(v.x))),
+                                           __float_as_uint(__fadd_rn(__uint_as_float(o.y), __uint_as_float(v.y))),
+                                           __float_as_uint(__fadd_rn(__uint_as_float(o.z), __uint_as_float(v.z))),
+                                           __float_as_uint(__fadd_rn(__uint_as_float(o.w), __uint_as_float(v.w))));
+                        } else {
+                            // out = bf16(float(out) + float(bf16(dW))): bf16 out.add_(dW)
+                            v.x = pack_bf16x2(__fadd_rn(bf16_lo(o.x), bf16_lo(v.x)), __fadd_rn(bf16_hi(o.x), bf16_hi(v.x)));
+                            v.y = pack_bf16x2(__fadd_rn(bf16_lo(o.y), bf16_lo(v.y)), __fadd_rn(bf16_hi(o.y), bf16_hi(v.y)));
+                            v.z = pack_bf16x2(__fadd_rn(bf16_lo(o.z), bf16_lo(v.z)), __fadd_rn(bf16_hi(o.z), bf16_hi(v.z)));
+                            v.w = pack_bf16x2(__fadd_rn(bf16_lo(o.w), bf16_lo(v.w)), __fadd_rn(bf16_hi(o.w), bf16_hi(v.w)));
+                        }
+                    }
+                    *reinterpret_cast<uint4*>(gline + 4 * j * ldo) = v;
+                }
+                __syncwarp();   // the box is rewritten by the next iteration
             }
-            if (!ok) break;
-            jg += static_cast<uint32_t>(nbox);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -736,11 +715,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 else mbar_arrive_cluster(tempty0 + buf * 8u);
             }
         }
-        // Every store has read its box and written HBM before the CTA leaves; after an abort,
-        // an old-value load may still be in flight: give it time to land.
-        if (lane == 0) bulk_wait_group<0>();
-        if (!ok && acc) spin_ns(kCopyDrainNs);
-        __syncwarp();
+        (void)ok;
     } else if (warp >= 4) {
         // ---------------------------------------------------------- fwd / dgrad epilogue
         const int q = warp & 3;                 // TMEM lanes [32q, 32q + 32)
