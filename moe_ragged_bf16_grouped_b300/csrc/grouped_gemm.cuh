@@ -712,7 +712,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 if (even) mbar_arrive(&c->tempty[buf]);
-                else mbar_arrive_cluster(tempty0 + buf * 8u);
+                else mbar_arrive_cluster_cta(tempty0 + buf * 8u);   // TMEM drained
             }
         }
         (void)ok;
@@ -756,7 +756,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 if (even) mbar_arrive(&c->tempty[buf]);
-                else mbar_arrive_cluster(tempty0 + buf * 8u);
+                else mbar_arrive_cluster_cta(tempty0 + buf * 8u);   // TMEM drained
             }
         }
     }

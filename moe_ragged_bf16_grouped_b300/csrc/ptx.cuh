@@ -230,9 +230,18 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (shared::cluster address).
+// Arrive on an mbarrier of another CTA of the cluster (shared::cluster address), releasing
+// this thread's earlier writes at cluster scope (it waits until they are visible there).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster with CTA-scope release only: for
+// signals that order tcgen05 work (through tcgen05 fences around the arrive and the wait)
+// rather than memory, so that the arrive does not wait for this thread's global stores.
+__device__ __forceinline__ void mbar_arrive_cluster_cta(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
 
