@@ -499,14 +499,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer (even CTA)
-        if (even) {
+        // One thread waits, issues and commits; the other lanes of the warp stay idle.
+        if (even && lane == 0) {
             int stage = 0, it = 0;
             uint32_t phase = 0;
             bool ok = true;
             for (int u = pair; u < total && ok; u += npairs, ++it) {
                 const Tile t = decode_unit<OP>(p, cu, sh, u);
                 const int buf = it & 1;
-                if (!wait_bar_warp(&c->tempty[buf], ((it >> 1) & 1) ^ 1u, c, pr, p.err)) {
+                if (!wait_bar(&c->tempty[buf], ((it >> 1) & 1) ^ 1u, c, pr, p.err)) {
                     ok = false;
                     break;
                 }
@@ -516,49 +517,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (OP != OP_WGRAD) row_split(t.ncols, n_mma, half, bi);
                 const uint32_t idesc = idesc_bf16(kPairM, static_cast<uint32_t>(n_mma),
                                                   OP != OP_FWD, OP == OP_WGRAD);
+                // K-major sub-tiles: 16-element steps are 32 B apart within a 64-wide block,
+                // blocks are sub-tile bytes apart.  MN-major: 16 reduction rows are 2 KB apart;
+                // the two 64-wide M/N blocks are kSubBytes apart (LBO).
+                const uint32_t b_sub = static_cast<uint32_t>((8 << bi) * 128);
                 for (int kb = 0; kb < t.nkb; ++kb) {
-                    if (!wait_bar_warp(&c->full[stage], phase, c, pr, p.err)) { ok = false; break; }
+                    if (!wait_bar(&c->full[stage], phase, c, pr, p.err)) { ok = false; break; }
                     tc_fence_after();
-                    uint8_t* a = smem + stage * kStageBytes;
+                    const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
+                    const uint32_t b_addr = a_addr + kABytes;
                     const int valid = t.nred - kb * kBK;
                     // fwd / dgrad: a last stage of 64 (K or N is a multiple of 64) skips the
                     // zero-filled second block.
-                    int nsteps = valid < kBK ? (valid + 15) >> 4 : kBK / 16;
-                    if (lane == 0) {
-                        const uint32_t a_addr = smem_u32(a), b_addr = a_addr + kABytes;
-                        // K-major sub-tiles: 16-element steps are 32 B apart within a 64-wide
-                        // block, blocks are sub-tile bytes apart.  MN-major: 16 reduction rows
-                        // are 2 KB apart; the two 64-wide M/N blocks are kSubBytes apart (LBO).
-                        const uint32_t b_sub = static_cast<uint32_t>((8 << bi) * 128);
-                        for (int kk = 0; kk < nsteps; ++kk) {
-                            const uint32_t kblk = static_cast<uint32_t>(kk >> 2), k16 = kk & 3;
-                            const uint64_t ad =
-                                (OP == OP_FWD)
-                                    ? sdesc_sw128(a_addr + kblk * kSubBytes + k16 * 32, 16, 1024)
-                                    : sdesc_sw128(a_addr + kk * 2048, kSubBytes, 1024);
-                            const uint64_t bd =
-                                (OP == OP_WGRAD)
-                                    ? sdesc_sw128(b_addr + kk * 2048, kSubBytes, 1024)
-                                    : sdesc_sw128(b_addr + kblk * b_sub + k16 * 32, 16, 1024);
-                            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
-                        }
-                        umma_commit_pair(&c->empty[stage], 3);
+                    const int nsteps = valid < kBK ? (valid + 15) >> 4 : kBK / 16;
+                    for (int kk = 0; kk < nsteps; ++kk) {
+                        const uint32_t kblk = static_cast<uint32_t>(kk >> 2), k16 = kk & 3;
+                        const uint64_t ad =
+                            (OP == OP_FWD)
+                                ? sdesc_sw128(a_addr + kblk * kSubBytes + k16 * 32, 16, 1024)
+                                : sdesc_sw128(a_addr + kk * 2048, kSubBytes, 1024);
+                        const uint64_t bd =
+                            (OP == OP_WGRAD)
+                                ? sdesc_sw128(b_addr + kk * 2048, kSubBytes, 1024)
+                                : sdesc_sw128(b_addr + kblk * b_sub + k16 * 32, 16, 1024);
+                        umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
                     }
-                    __syncwarp();
+                    umma_commit_pair(&c->empty[stage], 3);
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
                 // Arrives once this tile's MMAs (if any: an empty group has none) are done.
-                if (lane == 0) umma_commit_pair(&c->tfull[buf], 3);
-                __syncwarp();
+                umma_commit_pair(&c->tfull[buf], 3);
             }
             // Every MMA this thread issued has completed once this commit arrives.
-            if (lane == 0) {
-                umma_commit_pair(&c->drain, 1);
-                drain_wait(&c->drain, 0);
-            }
-            __syncwarp();
+            umma_commit_pair(&c->drain, 1);
+            drain_wait(&c->drain, 0);
         }
+        __syncwarp();
     } else if (warp == 3) {
         // ---------------------------------------------------------- wgrad tail fixer (both CTAs)
         if (OP == OP_WGRAD) {
