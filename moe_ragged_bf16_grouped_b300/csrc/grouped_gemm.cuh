@@ -339,16 +339,15 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, SmemCtl
     }
 }
 
-// Lane 0 waits (bounded); on success the other lanes then observe the completed phase
-// themselves, which cannot move on before this warp acts, so their waits return at once.
+// Lane 0 waits (bounded); __syncwarp then orders the rest of the warp after its acquire,
+// so the other lanes need not poll the barrier themselves.
 __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, SmemCtl* c,
                                               const Pair& pr, unsigned int* err) {
     const int lane = threadIdx.x & 31;
     int ok = 1;
     if (lane == 0) ok = wait_bar(bar, parity, c, pr, err);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok && lane != 0) ok = wait_bar(bar, parity, c, pr, err);
-    return __all_sync(0xffffffffu, ok) != 0;
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // Bounded wait that ignores the abort flag: used to let in-flight copies and MMAs land
