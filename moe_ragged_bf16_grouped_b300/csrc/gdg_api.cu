@@ -107,9 +107,9 @@ DeviceInfo g_dev[kMaxDevices];
 
 // Sets the kernel's shared-memory size and finds how many CTA pairs fit on the device at
 // once (the persistent grid).  The grid size never changes results, only speed.
-template <int OP, int EPI>
+template <int OP, int EPI, int RT>
 cudaError_t set_up_kernel(int sms, int* pairs) {
-    cudaError_t e = cudaFuncSetAttribute(gdg::grouped_gemm_kernel<OP, EPI>,
+    cudaError_t e = cudaFuncSetAttribute(gdg::grouped_gemm_kernel<OP, EPI, RT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(gdg::kGemmSmemBytes));
     if (e != cudaSuccess) return e;
@@ -126,7 +126,7 @@ cudaError_t set_up_kernel(int sms, int* pairs) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gdg::grouped_gemm_kernel<OP, EPI>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&n, gdg::grouped_gemm_kernel<OP, EPI, RT>, &cfg) != cudaSuccess ||
         n <= 0) {
         cudaGetLastError();
         n = sms / 2;
@@ -149,13 +149,15 @@ DeviceInfo* device_info(gdg_status* st) {
         void* err = nullptr;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaGetSymbolAddress(&err, g_device_error) != cudaSuccess ||
-            set_up_kernel<gdg::OP_FWD, gdg::EPI_BF16>(d.sms, &d.pairs) != cudaSuccess ||
-            set_up_kernel<gdg::OP_DGRAD, gdg::EPI_BF16>(d.sms, &d.pairs) != cudaSuccess ||
-            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_BF16>(d.sms, &d.pairs) != cudaSuccess ||
-            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_FP32>(d.sms, &d.pairs) != cudaSuccess ||
-            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_BF16_ACC>(d.sms, &d.pairs) != cudaSuccess ||
-            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_FP32_ACC>(d.sms, &d.pairs) != cudaSuccess ||
-            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_PARTIAL>(d.sms, &d.pairs) != cudaSuccess) {
+            set_up_kernel<gdg::OP_FWD, gdg::EPI_BF16, 256>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_FWD, gdg::EPI_BF16, 128>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_DGRAD, gdg::EPI_BF16, 256>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_DGRAD, gdg::EPI_BF16, 128>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_BF16, 256>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_FP32, 256>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_BF16_ACC, 256>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_FP32_ACC, 256>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_PARTIAL, 256>(d.sms, &d.pairs) != cudaSuccess) {
             *st = GDG_ECUDA;
             return nullptr;
         }
@@ -269,13 +271,21 @@ gdg_status run_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N,
     p.K = K;
     p.offs_kind = args->offs_kind;
     p.split_rows = 0;
+    // Row tile (and ring geometry), from the shapes alone: groups of at most 64 rows on
+    // average only stream weights, and a 128-row tile keeps more weight bytes in flight
+    // (larger groups lose more to re-reading weight tiles than they gain).
+    const int rt = (rows <= static_cast<int64_t>(E) * 64) ? 128 : 256;
     const int64_t ft = (OP == gdg::OP_FWD) ? N / gdg::kPairM : ceil_div(K, gdg::kPairM);
-    const int64_t ub = ft * (ceil_div(rows, gdg::kRowTile) + E);
+    const int64_t ub = ft * (ceil_div(rows, rt) + E);
     if (ub > INT32_MAX) return GDG_EINVAL;
     p.max_units = static_cast<int>(ub);
     const int grid = pair_grid(ub, dev->pairs);
-    gdg::grouped_gemm_kernel<OP, gdg::EPI_BF16><<<grid, gdg::kThreads, gdg::kGemmSmemBytes,
-                                   static_cast<cudaStream_t>(stream)>>>(p);
+    if (rt == 128)
+        gdg::grouped_gemm_kernel<OP, gdg::EPI_BF16, 128>
+            <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
+    else
+        gdg::grouped_gemm_kernel<OP, gdg::EPI_BF16, 256>
+            <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
     return launch_status(cudaGetLastError());
 }
 
@@ -384,23 +394,23 @@ gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int
     const int kepi = split ? static_cast<int>(gdg::EPI_PARTIAL) : epi;
     switch (kepi) {
         case gdg::EPI_BF16:
-            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_BF16>
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_BF16, 256>
                 <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
             break;
         case gdg::EPI_FP32:
-            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_FP32>
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_FP32, 256>
                 <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
             break;
         case gdg::EPI_BF16_ACC:
-            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_BF16_ACC>
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_BF16_ACC, 256>
                 <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
             break;
         case gdg::EPI_FP32_ACC:
-            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_FP32_ACC>
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_FP32_ACC, 256>
                 <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
             break;
         default:
-            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_PARTIAL>
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_PARTIAL, 256>
                 <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
             break;
     }

@@ -51,10 +51,23 @@ constexpr int kPairM = 256;                 // MMA M across the CTA pair
 constexpr int kBM = 128;                    // A rows (and D rows) per CTA
 constexpr int kBN = 256;                    // MMA N (max)
 constexpr int kBK = 128;                    // reduction elements per stage: two 64-wide blocks
-constexpr int kStages = 3;
 constexpr int kABytes = kBM * kBK * 2;      // 32 KB: this CTA's 128 rows of A
-constexpr int kBBytes = (kBN / 2) * kBK * 2;   // 32 KB: this CTA's half of B (<= 128 rows)
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kRingBytes = 3 * (kABytes + (kBN / 2) * kBK * 2);   // 192 KB operand ring
+constexpr int kMaxStages = 4;
+
+// Ring geometry, by the fwd / dgrad row tile RT (packed rows per tile): RT = 256 gives 3
+// stages of 64 KB (A 32 KB + B 32 KB per CTA); RT = 128 gives 4 stages of 48 KB (A 32 KB +
+// B 16 KB), i.e. a third more weight bytes in flight per SM for weight-streaming shapes.
+// wgrad always uses RT = 256 (its B half is 128 columns of X).
+template <int RT>
+struct Ring {
+    static constexpr int kRowTile = RT;
+    static constexpr int kStages = RT == 256 ? 3 : 4;
+    static constexpr int kBBytes = (RT / 2) * kBK * 2;      // this CTA's half of B
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static_assert(kStages * kStageBytes == kRingBytes, "ring geometries share 192 KB");
+    static_assert(kStages <= kMaxStages, "barrier arrays");
+};
 constexpr int kSubBytes = 128 * 128;        // one 128-row block of 64 bf16 (128 B) per row
 constexpr int kEpiWarps = 8;
 constexpr int kEpiBoxBytes = 32 * 128;      // wgrad staging box per warp: 32 rows x 128 B
@@ -63,7 +76,6 @@ constexpr int kThreads = 384;               // GEMM kernel: 4 role warps + 8 epi
 constexpr int kReduceThreads = 256;
 constexpr int kMaxE = 1024;
 constexpr int kTmemCols = 512;
-constexpr int kRowTile = 256;               // fwd / dgrad: packed rows per tile
 constexpr int kPartialElems = kPairM * kBN; // fp32 elements per split partial tile
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // any single wait > 2 s is a hang
 constexpr uint64_t kDrainLimitNs = 100000000ull;
@@ -93,10 +105,10 @@ struct GemmParams {
 };
 
 struct SmemCtl {
-    uint64_t full[kStages];     // even CTA: both CTAs' copies of a stage have landed (a wgrad
+    uint64_t full[kMaxStages];  // even CTA: both CTAs' copies of a stage have landed (a wgrad
                                 // tail stage: both CTAs' fixers have zeroed its tail rows)
-    uint64_t empty[kStages];    // both CTAs: the pair's MMAs have read the stage
-    uint64_t tail_full[kStages];   // both CTAs (wgrad): this CTA's copies of a tail stage
+    uint64_t empty[kMaxStages]; // both CTAs: the pair's MMAs have read the stage
+    uint64_t tail_full[kMaxStages];   // both CTAs (wgrad): this CTA's copies of a tail stage
     uint64_t tfull[2];          // both CTAs: the accumulator is complete
     uint64_t tempty[2];         // even CTA: all 16 epilogue warps of the pair drained it
     uint64_t drain;
@@ -107,7 +119,7 @@ struct SmemCtl {
 };
 
 constexpr size_t kGemmSmemBytes =
-    1024 + static_cast<size_t>(kStages) * kStageBytes + kEpiBytes + sizeof(SmemCtl);
+    1024 + static_cast<size_t>(kRingBytes) + kEpiBytes + sizeof(SmemCtl);
 
 // ------------------------------------------------------------------ schedule
 
@@ -138,13 +150,13 @@ __device__ __forceinline__ void group_range(const int32_t* offs, int kind, int64
     m = static_cast<int>(b - a);
 }
 
-template <int OP>
+template <int OP, int RT>
 __device__ __forceinline__ int units_of_group(int m, const Shape& sh, int split_rows) {
     if (OP == OP_WGRAD) {
         if (split_rows > 0) return ((m + split_rows - 1) / split_rows) * sh.ft;
         return sh.ft;       // every tile of every expert, empty groups included
     }
-    return ((m + kRowTile - 1) / kRowTile) * sh.ft;
+    return ((m + RT - 1) / RT) * sh.ft;
 }
 
 // Builds start/size/prefix/total in shared memory (ordered reduce of split partials).  Every
@@ -164,7 +176,7 @@ __device__ void build_schedule(const int32_t* offs, int kind, int64_t rows, int 
             group_range(offs, kind, rows, e, s, m);
             start[e] = s;
             size[e] = m;
-            v[j] = units_of_group<OP>(m, sh, split_rows);
+            v[j] = units_of_group<OP, 256>(m, sh, split_rows);
         }
         local += v[j];
     }
@@ -203,14 +215,14 @@ __device__ void build_schedule(const int32_t* offs, int kind, int64_t rows, int 
 
 // Number of work units over all groups, capped at max_units.  Every thread of the block
 // calls it.
-template <int OP>
+template <int OP, int RT>
 __device__ int count_units(const GemmParams& p, const Shape& sh, int* warp_tot) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int local = 0;
     for (int e = tid; e < p.E; e += kThreads) {
         int s, m;
         group_range(p.offs, p.offs_kind, p.rows, e, s, m);
-        local += units_of_group<OP>(m, sh, p.split_rows);
+        local += units_of_group<OP, RT>(m, sh, p.split_rows);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
@@ -227,25 +239,50 @@ struct Cursor {
     int e, base, n, s, m;
 };
 
-template <int OP>
+template <int OP, int RT>
 __device__ __forceinline__ void cursor_init(Cursor& cu, const GemmParams& p, const Shape& sh) {
     cu.e = 0;
     cu.base = 0;
     group_range(p.offs, p.offs_kind, p.rows, 0, cu.s, cu.m);
-    cu.n = units_of_group<OP>(cu.m, sh, p.split_rows);
+    cu.n = units_of_group<OP, RT>(cu.m, sh, p.split_rows);
 }
 
 // Moves the cursor to the group that holds unit u (u never decreases between calls, and
 // u < total, so the last group is never passed).
-template <int OP>
+template <int OP, int RT>
 __device__ __forceinline__ void cursor_seek(Cursor& cu, const GemmParams& p, const Shape& sh,
                                             int u) {
     while (u >= cu.base + cu.n && cu.e + 1 < p.E) {
         cu.base += cu.n;
         ++cu.e;
         group_range(p.offs, p.offs_kind, p.rows, cu.e, cu.s, cu.m);
-        cu.n = units_of_group<OP>(cu.m, sh, p.split_rows);
+        cu.n = units_of_group<OP, RT>(cu.m, sh, p.split_rows);
     }
+}
+
+// fp32 weight gradients of long groups: the tensor core's fp32 accumulator drifts by about
+// 0.7 ulp per MMA step, so a group longer than kChunkStages stages (2048 rows) is reduced in
+// chunks of that many rows, each accumulated fresh in one TMEM buffer and added (fp32,
+// round to nearest even, in chunk order) into a running sum kept in the other TMEM buffer.
+constexpr int kChunkStages = 16;
+
+// Times each of the two TMEM buffers has been handed to the epilogue (its tfull / tempty
+// phase count), in registers.
+struct Acq {
+    uint32_t n0 = 0, n1 = 0;
+    __device__ __forceinline__ uint32_t of(int b) const { return b ? n1 : n0; }
+    __device__ __forceinline__ void bump(int b) {
+        if (b) ++n1;
+        else ++n0;
+    }
+};
+
+template <int OP, int EPI>
+__device__ __forceinline__ int chunks_of(int nkb) {
+    constexpr bool chunked =
+        OP == OP_WGRAD && (EPI == EPI_FP32 || EPI == EPI_FP32_ACC || EPI == EPI_PARTIAL);
+    if (!chunked || nkb <= kChunkStages) return 1;
+    return (nkb + kChunkStages - 1) / kChunkStages;
 }
 
 // wgrad: a stage whose rows end inside a 16-row MMA step (rows of another group or split
@@ -264,10 +301,10 @@ struct Tile {
     int u;
 };
 
-template <int OP>
+template <int OP, int RT>
 __device__ __forceinline__ Tile decode_unit(const GemmParams& p, Cursor& cu, const Shape& sh,
                                             int u) {
-    cursor_seek<OP>(cu, p, sh, u);
+    cursor_seek<OP, RT>(cu, p, sh, u);
     Tile t;
     t.u = u;
     t.e = cu.e;
@@ -288,11 +325,11 @@ __device__ __forceinline__ Tile decode_unit(const GemmParams& p, Cursor& cu, con
             t.nred = m;
         }
     } else {
-        const int rc_n = (m + kRowTile - 1) / kRowTile;
+        const int rc_n = (m + RT - 1) / RT;
         const int ft = local / rc_n, rc = local - ft * rc_n;
         t.f0 = ft * kPairM;
-        t.c0 = s + rc * kRowTile;
-        t.ncols = min(kRowTile, m - rc * kRowTile);
+        t.c0 = s + rc * RT;
+        t.ncols = min(RT, m - rc * RT);
         t.r0 = 0;
         t.nred = (OP == OP_FWD) ? p.K : p.N;
     }
@@ -378,14 +415,16 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 // ------------------------------------------------------------------ the GEMM kernel
 
 // EPI: the epilogue (fwd / dgrad: EPI_BF16; wgrad: any, EPI_PARTIAL for the split form).
-template <int OP, int EPI>
+// RT: the fwd / dgrad row tile, which also picks the ring geometry (wgrad: 256).
+template <int OP, int EPI, int RT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     // Same offset in both CTAs of the pair: the MMA reads A and B of both at one address.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* stage_area = smem + kStages * kStageBytes;      // wgrad epilogue staging boxes
+    using R = Ring<RT>;
+    uint8_t* stage_area = smem + kRingBytes;                 // wgrad epilogue staging boxes
     SmemCtl* c = reinterpret_cast<SmemCtl*>(stage_area + kEpiBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -397,7 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < R::kStages; ++s) {
             // wgrad: a stage is released by two arrivals, the even producer's two (plain
             // stage) or one per CTA's fixer (tail stage).
             mbar_init(&c->full[s], OP == OP_WGRAD ? 2 : 1);
@@ -419,9 +458,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else
             for (int i = 0; i < 5; ++i) prefetch_tmap(&p.tmB[i]);
     }
-    const int total = count_units<OP>(p, sh, c->warp_tot);
+    const int total = count_units<OP, RT>(p, sh, c->warp_tot);
     Cursor cu;
-    cursor_init<OP>(cu, p, sh);
+    cursor_init<OP, RT>(cu, p, sh);
     // Both CTAs' barriers are initialised (and the peer has started) before any CTA signals
     // the other's barriers or allocates TMEM together with it.
     cluster_sync();
@@ -443,11 +482,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int u = pair; u < total && ok; u += npairs) {
-                const Tile t = decode_unit<OP>(p, cu, sh, u);
+                const Tile t = decode_unit<OP, RT>(p, cu, sh, u);
                 int n_mma = 0, half = 0, bi = 0;
                 if (OP != OP_WGRAD) row_split(t.ncols, n_mma, half, bi);
                 const uint32_t bytes = (OP == OP_WGRAD)
-                                           ? 2u * (kABytes + kBBytes)
+                                           ? 2u * (kABytes + R::kBBytes)
                                            : 2u * (kABytes + (8u << bi) * 256u);
                 const int fa = t.f0 + kBM * static_cast<int>(pr.rank);   // this CTA's A rows
                 if (OP == OP_WGRAD && (EPI == EPI_FP32_ACC || EPI == EPI_BF16_ACC))
@@ -456,14 +495,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tma_prefetch_2d(&p.tmPre, t.c0, t.e * p.N + fa);
                 for (int kb = 0; kb < t.nkb; ++kb) {
                     if (!wait_bar(&c->empty[stage], phase ^ 1u, c, pr, p.err)) { ok = false; break; }
-                    uint8_t* a = smem + stage * kStageBytes;
+                    uint8_t* a = smem + stage * R::kStageBytes;
                     uint8_t* b = a + kABytes;
                     uint32_t fb = full0 + stage * 8u;
                     if (OP == OP_WGRAD && needs_fix(t.nred - kb * kBK)) {
                         // Tail stage: this CTA's copies complete on its own barrier; its fixer
                         // zeroes the rows past the group end, then releases the stage.
                         fb = tail0 + stage * 8u;
-                        mbar_arrive_expect_tx(&c->tail_full[stage], kABytes + kBBytes);
+                        mbar_arrive_expect_tx(&c->tail_full[stage], kABytes + R::kBBytes);
                     } else if (even) {
                         mbar_arrive_expect_tx(&c->full[stage], bytes);
                         if (OP == OP_WGRAD) mbar_arrive(&c->full[stage]);
@@ -488,7 +527,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         tma_load_3d_pair(b, &p.tmB[0], fb, 0, r,
                                          (t.c0 + (kBN / 2) * static_cast<int>(pr.rank)) / 64);
                     }
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    if (++stage == R::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
             // After an abort, let every copy this thread started land before the CTA exits.
@@ -499,19 +538,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer (even CTA)
         // One thread waits, issues and commits; the other lanes of the warp stay idle.
+        // TMEM buffers alternate between units; acq counts the times each buffer has been
+        // handed to the epilogue (its tfull / tempty phase).  A chunked unit keeps buffer A
+        // for its chunks and hands buffer B to the epilogue for the running sum.
         if (even && lane == 0) {
-            int stage = 0, it = 0;
+            int stage = 0, nextb = 0;
             uint32_t phase = 0;
+            Acq acq;
             bool ok = true;
-            for (int u = pair; u < total && ok; u += npairs, ++it) {
-                const Tile t = decode_unit<OP>(p, cu, sh, u);
-                const int buf = it & 1;
-                if (!wait_bar(&c->tempty[buf], ((it >> 1) & 1) ^ 1u, c, pr, p.err)) {
-                    ok = false;
-                    break;
+            for (int u = pair; u < total && ok; u += npairs) {
+                const Tile t = decode_unit<OP, RT>(p, cu, sh, u);
+                const int nch = chunks_of<OP, EPI>(t.nkb);
+                const int A = nextb, B = nextb ^ 1;
+                if (nch > 1) {
+                    // The running-sum buffer: once its previous use is drained, hand it over
+                    // (the commit arrives when every MMA issued so far is done).
+                    if (!wait_bar(&c->tempty[B], (acq.of(B) & 1u) ^ 1u, c, pr, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    umma_commit_pair(&c->tfull[B], 3);
+                    acq.bump(B);
                 }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kBN);
                 int n_mma = kBN, half = 0, bi = 0;
                 if (OP != OP_WGRAD) row_split(t.ncols, n_mma, half, bi);
                 const uint32_t idesc = idesc_bf16(kPairM, static_cast<uint32_t>(n_mma),
@@ -520,33 +566,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // blocks are sub-tile bytes apart.  MN-major: 16 reduction rows are 2 KB apart;
                 // the two 64-wide M/N blocks are kSubBytes apart (LBO).
                 const uint32_t b_sub = static_cast<uint32_t>((8 << bi) * 128);
-                for (int kb = 0; kb < t.nkb; ++kb) {
-                    if (!wait_bar(&c->full[stage], phase, c, pr, p.err)) { ok = false; break; }
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(A * kBN);
+                for (int ch = 0; ch < nch && ok; ++ch) {
+                    if (!wait_bar(&c->tempty[A], (acq.of(A) & 1u) ^ 1u, c, pr, p.err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
-                    const uint32_t b_addr = a_addr + kABytes;
-                    const int valid = t.nred - kb * kBK;
-                    // fwd / dgrad: a last stage of 64 (K or N is a multiple of 64) skips the
-                    // zero-filled second block.
-                    const int nsteps = valid < kBK ? (valid + 15) >> 4 : kBK / 16;
-                    for (int kk = 0; kk < nsteps; ++kk) {
-                        const uint32_t kblk = static_cast<uint32_t>(kk >> 2), k16 = kk & 3;
-                        const uint64_t ad =
-                            (OP == OP_FWD)
-                                ? sdesc_sw128(a_addr + kblk * kSubBytes + k16 * 32, 16, 1024)
-                                : sdesc_sw128(a_addr + kk * 2048, kSubBytes, 1024);
-                        const uint64_t bd =
-                            (OP == OP_WGRAD)
-                                ? sdesc_sw128(b_addr + kk * 2048, kSubBytes, 1024)
-                                : sdesc_sw128(b_addr + kblk * b_sub + k16 * 32, 16, 1024);
-                        umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                    const int kb0 = ch * kChunkStages;
+                    const int kb1 = nch > 1 ? min(t.nkb, kb0 + kChunkStages) : t.nkb;
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!wait_bar(&c->full[stage], phase, c, pr, p.err)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_u32(smem + stage * R::kStageBytes);
+                        const uint32_t b_addr = a_addr + kABytes;
+                        const int valid = t.nred - kb * kBK;
+                        // fwd / dgrad: a last stage of 64 (K or N is a multiple of 64) skips
+                        // the zero-filled second block.
+                        const int nsteps = valid < kBK ? (valid + 15) >> 4 : kBK / 16;
+                        for (int kk = 0; kk < nsteps; ++kk) {
+                            const uint32_t kblk = static_cast<uint32_t>(kk >> 2), k16 = kk & 3;
+                            const uint64_t ad =
+                                (OP == OP_FWD)
+                                    ? sdesc_sw128(a_addr + kblk * kSubBytes + k16 * 32, 16, 1024)
+                                    : sdesc_sw128(a_addr + kk * 2048, kSubBytes, 1024);
+                            const uint64_t bd =
+                                (OP == OP_WGRAD)
+                                    ? sdesc_sw128(b_addr + kk * 2048, kSubBytes, 1024)
+                                    : sdesc_sw128(b_addr + kblk * b_sub + k16 * 32, 16, 1024);
+                            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+                        }
+                        umma_commit_pair(&c->empty[stage], 3);
+                        if (++stage == R::kStages) { stage = 0; phase ^= 1u; }
                     }
-                    umma_commit_pair(&c->empty[stage], 3);
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    if (!ok) break;
+                    // Arrives once this chunk's MMAs (if any: an empty group has none) are done.
+                    umma_commit_pair(&c->tfull[A], 3);
+                    acq.bump(A);
                 }
-                if (!ok) break;
-                // Arrives once this tile's MMAs (if any: an empty group has none) are done.
-                umma_commit_pair(&c->tfull[buf], 3);
+                if (nch == 1) nextb ^= 1;
             }
             // Every MMA this thread issued has completed once this commit arrives.
             umma_commit_pair(&c->drain, 1);
@@ -561,7 +616,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t tphase = 0;     // per stage: parity of the next tail_full phase
             bool ok = true;
             for (int u = pair; u < total && ok; u += npairs) {
-                const Tile t = decode_unit<OP>(p, cu, sh, u);
+                const Tile t = decode_unit<OP, RT>(p, cu, sh, u);
                 for (int kb = 0; kb < t.nkb; ++kb) {
                     const int valid = t.nred - kb * kBK;
                     if (needs_fix(valid)) {
@@ -577,7 +632,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         // its 16-byte chunks does not matter.
                         // Lane l zeroes 16-byte chunk l % 8 of rows valid + l / 8, +4, ...
                         const int zend = (valid + 15) & ~15;
-                        uint8_t* base = smem + stage * kStageBytes + (lane & 7) * 16;
+                        uint8_t* base = smem + stage * R::kStageBytes + (lane & 7) * 16;
 #pragma unroll
                         for (int bx = 0; bx < 4; ++bx)
                             for (int r = valid + (lane >> 3); r < zend; r += 4)
@@ -591,7 +646,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                         __syncwarp();
                     }
-                    if (++stage == kStages) stage = 0;
+                    if (++stage == R::kStages) stage = 0;
                 }
             }
         }
@@ -616,14 +671,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint8_t* wslot = box + lane * 128;              // this lane's row in the write phase
         const int wsw = lane & 7;
         bool ok = true;
-        int it = 0;
-        for (int u = pair; u < total; u += npairs, ++it) {
-            const Tile t = decode_unit<OP>(p, cu, sh, u);
-            const int buf = it & 1;
-            if (!wait_bar_warp(&c->tfull[buf], (it >> 1) & 1, c, pr, p.err)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(buf * kBN);
+        int nextb = 0;
+        Acq acq;                        // the MMA issuer's buffer plan, followed step by step
+        for (int u = pair; u < total && ok; u += npairs) {
+            const Tile t = decode_unit<OP, RT>(p, cu, sh, u);
+            const int nch = chunks_of<OP, EPI>(t.nkb);
+            const int A = nextb, B = nextb ^ 1;
+            const uint32_t lanebase = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+            const int cend = min(128 * hc + 128, t.ncols);
+            int fb = A;                 // the buffer that ends up holding the unit's value
+            if (nch > 1) {
+                // Chunked unit: B receives chunk 0, then B = RN(B + chunk c) for c = 1, 2, ...
+                if (!wait_bar_warp(&c->tfull[B], acq.of(B) & 1u, c, pr, p.err)) { ok = false; break; }
+                tc_fence_after();
+                acq.bump(B);
+                for (int ch = 0; ch < nch; ++ch) {
+                    if (!wait_bar_warp(&c->tfull[A], acq.of(A) & 1u, c, pr, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    for (int cb = 128 * hc; cb < cend; cb += 32) {
+                        uint32_t ra[32], rb[32];
+                        tmem_ld_32x32b_x32(lanebase + static_cast<uint32_t>(A * kBN + cb), ra);
+                        if (ch > 0) tmem_ld_32x32b_x32(lanebase + static_cast<uint32_t>(B * kBN + cb), rb);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            rb[j] = ch > 0 ? __float_as_uint(__fadd_rn(__uint_as_float(rb[j]),
+                                                                      __uint_as_float(ra[j])))
+                                           : ra[j];
+                        tmem_st_32x32b_x32(lanebase + static_cast<uint32_t>(B * kBN + cb), rb);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (even) mbar_arrive(&c->tempty[A]);
+                        else mbar_arrive_cluster_cta(tempty0 + A * 8u);   // chunk drained
+                    }
+                    acq.bump(A);
+                }
+                if (!ok) break;
+                fb = B;
+            } else {
+                if (!wait_bar_warp(&c->tfull[A], acq.of(A) & 1u, c, pr, p.err)) { ok = false; break; }
+                tc_fence_after();
+                acq.bump(A);
+            }
+            const uint32_t taddr = lanebase + static_cast<uint32_t>(fb * kBN);
             uint8_t* obase;
             size_t ldo;
             if (EPI == EPI_PARTIAL) {
@@ -636,7 +729,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         (static_cast<size_t>(t.e) * p.N + t.f0 + mrow0) * ldo +
                         static_cast<size_t>(t.c0) * osz;
             }
-            const int cend = min(128 * hc + 128, t.ncols);
             for (int cb = 128 * hc; cb < cend; cb += box_cols) {
                 uint8_t* gline = obase + static_cast<size_t>(rr) * ldo + cb * osz + gg * 16;
                 uint4 old[8];
@@ -705,9 +797,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                if (even) mbar_arrive(&c->tempty[buf]);
-                else mbar_arrive_cluster_cta(tempty0 + buf * 8u);   // TMEM drained
+                if (even) mbar_arrive(&c->tempty[fb]);
+                else mbar_arrive_cluster_cta(tempty0 + fb * 8u);   // TMEM drained
             }
+            if (nch == 1) nextb ^= 1;
         }
         (void)ok;
     } else if (warp >= 4) {
@@ -718,7 +811,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t tempty0 = mapa_shared(smem_u32(&c->tempty[0]), 0u);
         int it = 0;
         for (int u = pair; u < total; u += npairs, ++it) {
-            const Tile t = decode_unit<OP>(p, cu, sh, u);
+            const Tile t = decode_unit<OP, RT>(p, cu, sh, u);
             const int buf = it & 1;
             if (!wait_bar_warp(&c->tfull[buf], (it >> 1) & 1, c, pr, p.err)) break;
             tc_fence_after();

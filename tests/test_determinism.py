@@ -12,7 +12,7 @@ DEV = "cuda"
 
 def test_ten_runs_bitwise(cuda_lib):
     w = wl.Workload("det", E=7, N=512, K=384, ops=(), main_grad_std=0.01)
-    h, d = inputs_on(w, DEV, seed=5, sizes=[900, 0, 1, 333, 64, 1500, 17])
+    h, d = inputs_on(w, DEV, seed=5, sizes=[900, 0, 1, 333, 64, 2600, 17])
     runs = {k: [] for k in ("fwd", "dgrad", "w16", "w32", "split", "acc")}
     for _ in range(10):
         runs["fwd"].append(cuda_lib.grouped_det_gemm_fwd(d["X"], d["W"], d["offs"]))

@@ -25,6 +25,10 @@ SMALL = [
     ("indptr_lead", 5, 256, 448, [0, 129, 64, 0, 700], 3, 2, wl.OFFS_INDPTR),
     ("one_group", 1, 768, 192, [1000], 0, 0, wl.OFFS_ENDS),
     ("all_tiny_groups", 40, 256, 128, [i % 4 for i in range(40)], 0, 1, wl.OFFS_ENDS),
+    # more than 64 rows per group on average: fwd / dgrad take the 256-row tile
+    ("big_groups", 3, 512, 320, [700, 1, 601], 0, 3, wl.OFFS_ENDS),
+    # groups longer than 2048 rows: an fp32 weight gradient is reduced in 2048-row chunks
+    ("long_groups", 3, 256, 128, [5000, 3, 2100], 0, 0, wl.OFFS_ENDS),
 ]
 
 
@@ -100,11 +104,14 @@ def test_wgrad_accumulate(cuda_lib, spec, split_rows):
     assert_bitwise(fused16, mg16.clone().add_(dW16), "bf16 accumulate vs add_")
 
 
-def test_integer_exact_bitwise(cuda_lib):
+@pytest.mark.parametrize("sizes", [[37, 0, 1, 30, 64], [300, 333]],
+                         ids=["row_tile_128", "row_tile_256"])
+def test_integer_exact_bitwise(cuda_lib, sizes):
     """Small-integer operands: every partial sum is exact in fp32 and the results are
-    exact in bf16, so every summation order gives the oracle's value exactly."""
-    E, N, K = 5, 256, 192
-    sizes = [37, 0, 1, 130, 64]
+    exact in bf16, so every summation order gives the oracle's value exactly.  The two size
+    lists put fwd / dgrad on the 128-row and on the 256-row tile (average group size at most
+    or above 64 rows)."""
+    E, N, K = len(sizes), 256, 192
     rows = sum(sizes) + 3
     X = wl.integer_bf16((rows, K), -2, 2, seed=3, tag=1)
     G = wl.integer_bf16((rows, N), -2, 2, seed=3, tag=2)
