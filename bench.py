@@ -387,7 +387,7 @@ def run_reference(args, world, rank):
     d = wl.make_inputs(w, seed=0, device="cpu", need=("X", "W", "G"))
     hb = host_bits(d)
     log(f"reference arm: inputs generated in {time.perf_counter() - t0:.1f} s")
-    budget = 120.0 / max(1, args.steps + args.warmup)   # whole run within a few minutes
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)   # whole run within a few minutes
     n_f, n_d, n_w = scaled_sample(hb, budget)
     for _ in range(args.warmup):
         oracle_sample_time(hb, n_f, n_d, n_w)
@@ -420,6 +420,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="reference arm: oracle seconds for the whole run (warm-up + timed steps)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
