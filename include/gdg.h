@@ -149,6 +149,35 @@ GDG_API const char* gdg_status_string(gdg_status status);
  * GDG_ETIMEOUT) and clears it. */
 GDG_API gdg_status gdg_device_error(void);
 
+/*
+ * Prepared launches (docs page, "Prepared launches": validate and bind once, then launch any
+ * number of times).  gdg_plan_create runs every check of the matching entry point
+ * (op = GDG_OP_FWD, GDG_OP_DGRAD or GDG_OP_WGRAD, the same arguments) and binds the result:
+ * the kernel form, the encoded tensor maps of the given buffers and the grid.  On failure it
+ * returns the entry point's status and sets *plan to NULL.  The plan lives in host memory
+ * (the library allocates no device memory) until gdg_plan_destroy.
+ *
+ * gdg_plan_launch enqueues exactly what the entry point would, on the given stream, with no
+ * other host work: it allocates nothing, never synchronises and may be captured in a CUDA
+ * graph.  The buffers bound at creation must stay allocated while the plan is used; new
+ * offsets or operand values written into them are honoured by every later launch or graph
+ * replay, and with accumulate every launch or replay adds again.  The offsets must still
+ * describe groups inside the bound rows.  A plan is read-only during launches, so one plan
+ * may be launched from several threads; launches that overlap on the GPU and write the same
+ * output race like any two kernels writing one buffer.  The first create or call on a device
+ * does that device's set-up (kernel attributes, occupancy query): make it before a capture.
+ */
+typedef struct gdg_plan gdg_plan;
+
+GDG_API gdg_status gdg_plan_create(int op, const gdg_args* args, const int32_t* offs, int E, int N,
+                                   int K, gdg_dtype out_dtype, int accumulate, gdg_plan** plan);
+
+/* NULL plan: GDG_EINVAL.  A launch failure: GDG_ECUDA. */
+GDG_API gdg_status gdg_plan_launch(const gdg_plan* plan, void* stream);
+
+/* Frees a plan (NULL is ignored).  Must not race with a launch of the same plan. */
+GDG_API void gdg_plan_destroy(gdg_plan* plan);
+
 /* Bytes of the library's own fixed scratch used by grouped_det_gemm_wgrad_noalloc. */
 #define GDG_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -25,7 +25,9 @@ __all__ = [
     "GDG_OFFS_ENDS", "GDG_OFFS_INDPTR", "GDG_OP_FWD", "GDG_OP_DGRAD", "GDG_OP_WGRAD",
     "GdgError", "grouped_det_gemm_fwd", "grouped_det_gemm_dgrad", "grouped_det_gemm_wgrad",
     "grouped_det_gemm_workspace_bytes", "grouped_det_gemm_auto_split_rows",
-    "grouped_det_gemm_wgrad_noalloc", "GDG_NOALLOC_SCRATCH_BYTES",
+    "grouped_det_gemm_wgrad_noalloc", "GDG_NOALLOC_SCRATCH_BYTES", "GroupedDetGemmPlan",
+    "prepare_grouped_det_gemm_fwd", "prepare_grouped_det_gemm_dgrad",
+    "prepare_grouped_det_gemm_wgrad",
     "gdg_status_string", "gdg_device_error", "library_path",
 ]
 
@@ -65,6 +67,14 @@ _lib.gdg_status_string.restype = ctypes.c_char_p
 _lib.gdg_status_string.argtypes = [ctypes.c_int]
 _lib.gdg_device_error.restype = ctypes.c_int
 _lib.gdg_device_error.argtypes = []
+_lib.gdg_plan_create.restype = ctypes.c_int
+_lib.gdg_plan_create.argtypes = [ctypes.c_int, ctypes.POINTER(GdgArgs), ctypes.c_void_p,
+                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                 ctypes.c_int, ctypes.POINTER(ctypes.c_void_p)]
+_lib.gdg_plan_launch.restype = ctypes.c_int
+_lib.gdg_plan_launch.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+_lib.gdg_plan_destroy.restype = None
+_lib.gdg_plan_destroy.argtypes = [ctypes.c_void_p]
 
 
 def library_path() -> str:
@@ -141,16 +151,12 @@ def _stream_ptr(stream, device) -> int:
 
 
 def _call(fn, name, args, offs, E, N, K, dtype_code, accumulate, stream):
-    st = fn(ctypes.byref(args), offs.data_ptr(), E, N, K, dtype_code, accumulate, stream)
+    st = fn(ctypes.byref(args), offs.data_ptr(), E, N, K, dtype_code, int(accumulate), stream)
     if st != GDG_OK:
         raise GdgError(st, name)
 
 
-def grouped_det_gemm_fwd(x: torch.Tensor, w: torch.Tensor, offs: torch.Tensor,
-                         out: torch.Tensor | None = None, *, offs_kind=GDG_OFFS_ENDS,
-                         stream=None) -> torch.Tensor:
-    """Y[rows, N] with Y[g] = X[g] @ W[e].T for every group (rows outside all groups
-    are left as they are in ``out``)."""
+def _fwd_args(x, w, offs, out, offs_kind):
     kind = _offs_kind(offs_kind)
     _check_operand(x, "x", ndim=2)
     _check_operand(w, "w", ndim=3)
@@ -163,15 +169,10 @@ def grouped_det_gemm_fwd(x: torch.Tensor, w: torch.Tensor, offs: torch.Tensor,
     if tuple(out.shape) != (x.shape[0], N):
         raise ValueError("out must be [rows, N]")
     args = GdgArgs(x.data_ptr(), w.data_ptr(), out.data_ptr(), None, 0, x.shape[0], kind, 0)
-    _call(_lib.grouped_det_gemm_fwd, "grouped_det_gemm_fwd", args, offs, E, N, K, GDG_BF16, 0,
-          _stream_ptr(stream, x.device))
-    return out
+    return args, (E, N, K, GDG_BF16, 0), out, (x, w, offs, out)
 
 
-def grouped_det_gemm_dgrad(g: torch.Tensor, w: torch.Tensor, offs: torch.Tensor,
-                           out: torch.Tensor | None = None, *, offs_kind=GDG_OFFS_ENDS,
-                           stream=None) -> torch.Tensor:
-    """dX[rows, K] with dX[g] = G[g] @ W[e] (W as stored)."""
+def _dgrad_args(g, w, offs, out, offs_kind):
     kind = _offs_kind(offs_kind)
     _check_operand(g, "g", ndim=2)
     _check_operand(w, "w", ndim=3)
@@ -184,18 +185,11 @@ def grouped_det_gemm_dgrad(g: torch.Tensor, w: torch.Tensor, offs: torch.Tensor,
     if tuple(out.shape) != (g.shape[0], K):
         raise ValueError("out must be [rows, K]")
     args = GdgArgs(g.data_ptr(), w.data_ptr(), out.data_ptr(), None, 0, g.shape[0], kind, 0)
-    _call(_lib.grouped_det_gemm_dgrad, "grouped_det_gemm_dgrad", args, offs, E, N, K, GDG_BF16,
-          0, _stream_ptr(stream, g.device))
-    return out
+    return args, (E, N, K, GDG_BF16, 0), out, (g, w, offs, out)
 
 
-def grouped_det_gemm_wgrad(g: torch.Tensor, x: torch.Tensor, offs: torch.Tensor,
-                           out: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
-                           num_groups: int | None = None, *, accumulate: bool = False,
-                           split_rows: int = 0, workspace: torch.Tensor | None = None,
-                           offs_kind=GDG_OFFS_ENDS, stream=None) -> torch.Tensor:
-    """dW[E, N, K] with dW[e] = G[g].T @ X[g]; with ``accumulate`` the result is added
-    into ``out`` (bitwise ``out.add_(dW)`` in out's dtype)."""
+def _wgrad_args(g, x, offs, out, out_dtype, num_groups, accumulate, split_rows, workspace,
+                offs_kind):
     kind = _offs_kind(offs_kind)
     _check_operand(g, "g", ndim=2)
     _check_operand(x, "x", ndim=2)
@@ -224,9 +218,98 @@ def grouped_det_gemm_wgrad(g: torch.Tensor, x: torch.Tensor, offs: torch.Tensor,
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     args = GdgArgs(g.data_ptr(), x.data_ptr(), out.data_ptr(), ws_ptr, ws_bytes, rows, kind,
                    split_rows)
-    _call(_lib.grouped_det_gemm_wgrad, "grouped_det_gemm_wgrad", args, offs, E, N, K, code,
-          int(accumulate), _stream_ptr(stream, g.device))
+    return args, (E, N, K, code, int(accumulate)), out, (g, x, offs, out, workspace)
+
+
+def grouped_det_gemm_fwd(x: torch.Tensor, w: torch.Tensor, offs: torch.Tensor,
+                         out: torch.Tensor | None = None, *, offs_kind=GDG_OFFS_ENDS,
+                         stream=None) -> torch.Tensor:
+    """Y[rows, N] with Y[g] = X[g] @ W[e].T for every group (rows outside all groups
+    are left as they are in ``out``)."""
+    args, dims, out, _ = _fwd_args(x, w, offs, out, offs_kind)
+    _call(_lib.grouped_det_gemm_fwd, "grouped_det_gemm_fwd", args, offs, *dims,
+          _stream_ptr(stream, x.device))
     return out
+
+
+def grouped_det_gemm_dgrad(g: torch.Tensor, w: torch.Tensor, offs: torch.Tensor,
+                           out: torch.Tensor | None = None, *, offs_kind=GDG_OFFS_ENDS,
+                           stream=None) -> torch.Tensor:
+    """dX[rows, K] with dX[g] = G[g] @ W[e] (W as stored)."""
+    args, dims, out, _ = _dgrad_args(g, w, offs, out, offs_kind)
+    _call(_lib.grouped_det_gemm_dgrad, "grouped_det_gemm_dgrad", args, offs, *dims,
+          _stream_ptr(stream, g.device))
+    return out
+
+
+def grouped_det_gemm_wgrad(g: torch.Tensor, x: torch.Tensor, offs: torch.Tensor,
+                           out: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
+                           num_groups: int | None = None, *, accumulate: bool = False,
+                           split_rows: int = 0, workspace: torch.Tensor | None = None,
+                           offs_kind=GDG_OFFS_ENDS, stream=None) -> torch.Tensor:
+    """dW[E, N, K] with dW[e] = G[g].T @ X[g]; with ``accumulate`` the result is added
+    into ``out`` (bitwise ``out.add_(dW)`` in out's dtype)."""
+    args, dims, out, _ = _wgrad_args(g, x, offs, out, out_dtype, num_groups, accumulate,
+                                     split_rows, workspace, offs_kind)
+    _call(_lib.grouped_det_gemm_wgrad, "grouped_det_gemm_wgrad", args, offs, *dims,
+          _stream_ptr(stream, g.device))
+    return out
+
+
+class GroupedDetGemmPlan:
+    """A prepared launch (``gdg_plan_create``): the call's checks ran and its buffers, kernel
+    form and grid are bound.  ``launch()`` enqueues the call's kernels on a stream with no
+    other host work; it allocates nothing, never synchronises and can be captured in a CUDA
+    graph.  New values written into the bound tensors (offsets included) are honoured by every
+    later launch or replay; with accumulate each launch adds again.  The plan keeps its tensors
+    alive.  ``out`` is the bound output tensor."""
+
+    def __init__(self, op: int, args: GdgArgs, dims, offs: torch.Tensor, out: torch.Tensor,
+                 keep, name: str):
+        self.out = out
+        self._keep = keep
+        self._device = out.device
+        h = ctypes.c_void_p()
+        st = _lib.gdg_plan_create(op, ctypes.byref(args), offs.data_ptr(), *dims, ctypes.byref(h))
+        if st != GDG_OK:
+            raise GdgError(st, name)
+        self._h = h
+
+    def launch(self, stream=None) -> torch.Tensor:
+        st = _lib.gdg_plan_launch(self._h, _stream_ptr(stream, self._device))
+        if st != GDG_OK:
+            raise GdgError(st, "gdg_plan_launch")
+        return self.out
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            _lib.gdg_plan_destroy(h)
+            self._h = None
+
+
+def prepare_grouped_det_gemm_fwd(x, w, offs, out=None, *, offs_kind=GDG_OFFS_ENDS):
+    """Prepared form of grouped_det_gemm_fwd (same arguments)."""
+    args, dims, out, keep = _fwd_args(x, w, offs, out, offs_kind)
+    return GroupedDetGemmPlan(GDG_OP_FWD, args, dims, offs, out, keep, "prepare_grouped_det_gemm_fwd")
+
+
+def prepare_grouped_det_gemm_dgrad(g, w, offs, out=None, *, offs_kind=GDG_OFFS_ENDS):
+    """Prepared form of grouped_det_gemm_dgrad (same arguments)."""
+    args, dims, out, keep = _dgrad_args(g, w, offs, out, offs_kind)
+    return GroupedDetGemmPlan(GDG_OP_DGRAD, args, dims, offs, out, keep,
+                              "prepare_grouped_det_gemm_dgrad")
+
+
+def prepare_grouped_det_gemm_wgrad(g, x, offs, out=None, out_dtype=None, num_groups=None, *,
+                                   accumulate=False, split_rows=0, workspace=None,
+                                   offs_kind=GDG_OFFS_ENDS):
+    """Prepared form of grouped_det_gemm_wgrad (same arguments); the split form's workspace
+    is allocated here when not given and bound to the plan."""
+    args, dims, out, keep = _wgrad_args(g, x, offs, out, out_dtype, num_groups, accumulate,
+                                        split_rows, workspace, offs_kind)
+    return GroupedDetGemmPlan(GDG_OP_WGRAD, args, dims, offs, out, keep,
+                              "prepare_grouped_det_gemm_wgrad")
 
 
 def grouped_det_gemm_wgrad_noalloc(g: torch.Tensor, x: torch.Tensor, offs: torch.Tensor,

@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "gdg.h"
 #include "grouped_gemm.cuh"
@@ -233,14 +234,31 @@ gdg_status launch_status(cudaError_t e) {
     return GDG_ECUDA;
 }
 
+// A validated call with everything its launches need, bound once: the kernel variant, the
+// encoded tensor maps and parameters, and the grid.  Launching it does no host work beyond
+// the kernel launches, allocates nothing and never synchronises.
+struct Plan {
+    int op = 0;              // GDG_OP_*
+    int rt = 256;            // fwd / dgrad row tile (ring geometry)
+    int epi = 0;             // wgrad kernel's epilogue (EPI_PARTIAL for the split form)
+    bool launch = false;     // false: the call has nothing to launch (rows == 0 cases)
+    bool reduce = false;     // split form: ordered reduce of the partials after the GEMM
+    int grid = 0;
+    int rgrid = 0;
+    GemmParams p;
+    ReduceParams r;
+};
+
 // fwd (OP_FWD) and dgrad (OP_DGRAD) share everything but the operand maps.
 template <int OP>
-gdg_status run_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N, int K,
-                        gdg_dtype out_dtype, int accumulate, void* stream) {
+gdg_status plan_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N, int K,
+                         gdg_dtype out_dtype, int accumulate, Plan* pl) {
     gdg_status st = check_common(args, offs, E, N, K, out_dtype);
     if (st != GDG_OK) return st;
     if (out_dtype != GDG_BF16 || accumulate != 0 || args->split_rows != 0) return GDG_EINVAL;
     const int64_t rows = args->rows;
+    pl->op = OP;
+    pl->launch = false;
     if (rows == 0) return GDG_OK;
     if (!args->a || !args->b || !args->out) return GDG_EINVAL;
     if (!aligned16(args->a) || !aligned16(args->b) || !aligned16(args->out) || !aligned16(offs))
@@ -256,7 +274,7 @@ gdg_status run_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N,
     DeviceInfo* dev = device_info(&st);
     if (!dev) return st;
 
-    GemmParams p;
+    GemmParams& p = pl->p;
     std::memset(&p, 0, sizeof p);
     if (!encode_weight_blocks(&p.tmA, args->b, E, N, K)) return GDG_ECUDA;
     for (int i = 0; i < 5; ++i)
@@ -274,56 +292,18 @@ gdg_status run_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N,
     // Row tile (and ring geometry), from the shapes alone: groups of at most 64 rows on
     // average only stream weights, and a 128-row tile keeps more weight bytes in flight
     // (larger groups lose more to re-reading weight tiles than they gain).
-    const int rt = (rows <= static_cast<int64_t>(E) * 64) ? 128 : 256;
+    pl->rt = (rows <= static_cast<int64_t>(E) * 64) ? 128 : 256;
     const int64_t ft = (OP == gdg::OP_FWD) ? N / gdg::kPairM : ceil_div(K, gdg::kPairM);
-    const int64_t ub = ft * (ceil_div(rows, rt) + E);
+    const int64_t ub = ft * (ceil_div(rows, pl->rt) + E);
     if (ub > INT32_MAX) return GDG_EINVAL;
     p.max_units = static_cast<int>(ub);
-    const int grid = pair_grid(ub, dev->pairs);
-    if (rt == 128)
-        gdg::grouped_gemm_kernel<OP, gdg::EPI_BF16, 128>
-            <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
-    else
-        gdg::grouped_gemm_kernel<OP, gdg::EPI_BF16, 256>
-            <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
-    return launch_status(cudaGetLastError());
+    pl->grid = pair_grid(ub, dev->pairs);
+    pl->launch = true;
+    return GDG_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-gdg_status grouped_det_gemm_fwd(const gdg_args* args, const int32_t* offs, int E, int N, int K,
-                                gdg_dtype out_dtype, int accumulate, void* stream) {
-    return run_fwd_like<gdg::OP_FWD>(args, offs, E, N, K, out_dtype, accumulate, stream);
-}
-
-gdg_status grouped_det_gemm_dgrad(const gdg_args* args, const int32_t* offs, int E, int N,
-                                  int K, gdg_dtype out_dtype, int accumulate, void* stream) {
-    return run_fwd_like<gdg::OP_DGRAD>(args, offs, E, N, K, out_dtype, accumulate, stream);
-}
-
-int32_t grouped_det_gemm_auto_split_rows(int64_t rows, int E, int N, int K) {
-    if (E < 1 || N <= 0 || K <= 0 || N % 256 || K % 64 || rows < 0) return -1;
-    return auto_split_rows(rows, E, N, K);
-}
-
-size_t grouped_det_gemm_workspace_bytes(int op, int64_t rows, int E, int N, int K,
-                                        gdg_dtype out_dtype, int accumulate, int32_t split_rows) {
-    if (E < 1 || E > GDG_MAX_EXPERTS || N <= 0 || K <= 0 || rows < 0 || N % 256 || K % 64 ||
-        (out_dtype != GDG_BF16 && out_dtype != GDG_FP32) || op < GDG_OP_FWD || op > GDG_OP_WGRAD)
-        return static_cast<size_t>(-1);
-    (void)accumulate;
-    if (op != GDG_OP_WGRAD) return 0;
-    if (split_rows == 0) split_rows = auto_split_rows(rows, E, N, K);
-    if (split_rows < 0 || rows == 0) return 0;
-    if (split_rows % 64 != 0) return static_cast<size_t>(-1);
-    return static_cast<size_t>(split_max_units(rows, E, N, K, split_rows)) * gdg::kPartialElems *
-           sizeof(float);
-}
-
-gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int E, int N,
-                                  int K, gdg_dtype out_dtype, int accumulate, void* stream) {
+gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, int K,
+                      gdg_dtype out_dtype, int accumulate, Plan* pl) {
     gdg_status st = check_common(args, offs, E, N, K, out_dtype);
     if (st != GDG_OK) return st;
     if (accumulate != 0 && accumulate != 1) return GDG_EINVAL;
@@ -342,6 +322,8 @@ gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int
     const Range r_o = range_of(offs, static_cast<uint64_t>(E + args->offs_kind) * 4);
     if (overlaps(r_out, r_o) || (rows > 0 && (overlaps(r_out, r_a) || overlaps(r_out, r_b))))
         return GDG_EOVERLAP;
+    pl->op = GDG_OP_WGRAD;
+    pl->launch = false;
     if (rows == 0 && accumulate) return GDG_OK;   // nothing to add; out is left unchanged
 
     if (split_rows == 0) split_rows = auto_split_rows(rows, E, N, K);
@@ -365,7 +347,7 @@ gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int
 
     const int epi = accumulate ? (out_dtype == GDG_FP32 ? gdg::EPI_FP32_ACC : gdg::EPI_BF16_ACC)
                                : (out_dtype == GDG_FP32 ? gdg::EPI_FP32 : gdg::EPI_BF16);
-    GemmParams p;
+    GemmParams& p = pl->p;
     std::memset(&p, 0, sizeof p);
     // With rows == 0 no copy is ever issued; the maps still need a valid shape.
     const int64_t map_rows = rows > 0 ? rows : 1;
@@ -389,52 +371,153 @@ gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int
     p.offs_kind = args->offs_kind;
     p.split_rows = split ? split_rows : 0;
     p.max_units = static_cast<int>(max_units);
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int grid = pair_grid(max_units, dev->pairs);
-    const int kepi = split ? static_cast<int>(gdg::EPI_PARTIAL) : epi;
-    switch (kepi) {
+    pl->grid = pair_grid(max_units, dev->pairs);
+    pl->epi = split ? static_cast<int>(gdg::EPI_PARTIAL) : epi;
+    pl->launch = true;
+    pl->reduce = split;
+    if (split) {
+        ReduceParams& r = pl->r;
+        r.offs = offs;
+        r.partial = static_cast<const float*>(args->workspace);
+        r.out = args->out;
+        r.rows = rows;
+        r.E = E;
+        r.N = N;
+        r.K = K;
+        r.offs_kind = args->offs_kind;
+        r.epi = epi;
+        r.split_rows = split_rows;
+        r.max_units = static_cast<int>(max_units);
+        const int64_t vec4 = static_cast<int64_t>(E) * N * K / 4;
+        int64_t rgrid = ceil_div(vec4, gdg::kReduceThreads);
+        if (rgrid > static_cast<int64_t>(dev->sms) * 8) rgrid = static_cast<int64_t>(dev->sms) * 8;
+        pl->rgrid = static_cast<int>(rgrid);
+    }
+    return GDG_OK;
+}
+
+gdg_status launch_plan(const Plan& pl, cudaStream_t s) {
+    if (!pl.launch) return GDG_OK;
+    const GemmParams& p = pl.p;
+    const int g = pl.grid;
+    if (pl.op == GDG_OP_FWD) {
+        if (pl.rt == 128)
+            gdg::grouped_gemm_kernel<gdg::OP_FWD, gdg::EPI_BF16, 128><<<g, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+        else
+            gdg::grouped_gemm_kernel<gdg::OP_FWD, gdg::EPI_BF16, 256><<<g, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+        return launch_status(cudaGetLastError());
+    }
+    if (pl.op == GDG_OP_DGRAD) {
+        if (pl.rt == 128)
+            gdg::grouped_gemm_kernel<gdg::OP_DGRAD, gdg::EPI_BF16, 128><<<g, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+        else
+            gdg::grouped_gemm_kernel<gdg::OP_DGRAD, gdg::EPI_BF16, 256><<<g, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+        return launch_status(cudaGetLastError());
+    }
+    switch (pl.epi) {
         case gdg::EPI_BF16:
-            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_BF16, 256>
-                <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_BF16, 256><<<g, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
             break;
         case gdg::EPI_FP32:
-            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_FP32, 256>
-                <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_FP32, 256><<<g, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
             break;
         case gdg::EPI_BF16_ACC:
-            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_BF16_ACC, 256>
-                <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_BF16_ACC, 256><<<g, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
             break;
         case gdg::EPI_FP32_ACC:
-            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_FP32_ACC, 256>
-                <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_FP32_ACC, 256><<<g, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
             break;
         default:
-            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_PARTIAL, 256>
-                <<<grid, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_PARTIAL, 256><<<g, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
             break;
     }
-    st = launch_status(cudaGetLastError());
-    if (st != GDG_OK || !split) return st;
-
-    ReduceParams r;
-    r.offs = offs;
-    r.partial = static_cast<const float*>(args->workspace);
-    r.out = args->out;
-    r.rows = rows;
-    r.E = E;
-    r.N = N;
-    r.K = K;
-    r.offs_kind = args->offs_kind;
-    r.epi = epi;
-    r.split_rows = split_rows;
-    r.max_units = static_cast<int>(max_units);
-    const int64_t vec4 = static_cast<int64_t>(E) * N * K / 4;
-    int64_t rgrid = ceil_div(vec4, gdg::kReduceThreads);
-    if (rgrid > static_cast<int64_t>(dev->sms) * 8) rgrid = static_cast<int64_t>(dev->sms) * 8;
-    gdg::wgrad_reduce_kernel<<<static_cast<int>(rgrid), gdg::kReduceThreads, 0, s>>>(r);
+    gdg_status st = launch_status(cudaGetLastError());
+    if (st != GDG_OK || !pl.reduce) return st;
+    gdg::wgrad_reduce_kernel<<<pl.rgrid, gdg::kReduceThreads, 0, s>>>(pl.r);
     return launch_status(cudaGetLastError());
 }
+
+gdg_status make_plan(int op, const gdg_args* args, const int32_t* offs, int E, int N, int K,
+                     gdg_dtype out_dtype, int accumulate, Plan* pl) {
+    switch (op) {
+        case GDG_OP_FWD: return plan_fwd_like<gdg::OP_FWD>(args, offs, E, N, K, out_dtype, accumulate, pl);
+        case GDG_OP_DGRAD: return plan_fwd_like<gdg::OP_DGRAD>(args, offs, E, N, K, out_dtype, accumulate, pl);
+        case GDG_OP_WGRAD: return plan_wgrad(args, offs, E, N, K, out_dtype, accumulate, pl);
+    }
+    return GDG_EINVAL;
+}
+
+gdg_status run(int op, const gdg_args* args, const int32_t* offs, int E, int N, int K,
+               gdg_dtype out_dtype, int accumulate, void* stream) {
+    Plan pl;
+    const gdg_status st = make_plan(op, args, offs, E, N, K, out_dtype, accumulate, &pl);
+    if (st != GDG_OK) return st;
+    return launch_plan(pl, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+gdg_status grouped_det_gemm_fwd(const gdg_args* args, const int32_t* offs, int E, int N, int K,
+                                gdg_dtype out_dtype, int accumulate, void* stream) {
+    return run(GDG_OP_FWD, args, offs, E, N, K, out_dtype, accumulate, stream);
+}
+
+gdg_status grouped_det_gemm_dgrad(const gdg_args* args, const int32_t* offs, int E, int N,
+                                  int K, gdg_dtype out_dtype, int accumulate, void* stream) {
+    return run(GDG_OP_DGRAD, args, offs, E, N, K, out_dtype, accumulate, stream);
+}
+
+int32_t grouped_det_gemm_auto_split_rows(int64_t rows, int E, int N, int K) {
+    if (E < 1 || N <= 0 || K <= 0 || N % 256 || K % 64 || rows < 0) return -1;
+    return auto_split_rows(rows, E, N, K);
+}
+
+size_t grouped_det_gemm_workspace_bytes(int op, int64_t rows, int E, int N, int K,
+                                        gdg_dtype out_dtype, int accumulate, int32_t split_rows) {
+    if (E < 1 || E > GDG_MAX_EXPERTS || N <= 0 || K <= 0 || rows < 0 || N % 256 || K % 64 ||
+        (out_dtype != GDG_BF16 && out_dtype != GDG_FP32) || op < GDG_OP_FWD || op > GDG_OP_WGRAD)
+        return static_cast<size_t>(-1);
+    (void)accumulate;
+    if (op != GDG_OP_WGRAD) return 0;
+    if (split_rows == 0) split_rows = auto_split_rows(rows, E, N, K);
+    if (split_rows < 0 || rows == 0) return 0;
+    if (split_rows % 64 != 0) return static_cast<size_t>(-1);
+    return static_cast<size_t>(split_max_units(rows, E, N, K, split_rows)) * gdg::kPartialElems *
+           sizeof(float);
+}
+
+gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int E, int N,
+                                  int K, gdg_dtype out_dtype, int accumulate, void* stream) {
+    return run(GDG_OP_WGRAD, args, offs, E, N, K, out_dtype, accumulate, stream);
+}
+
+struct gdg_plan {
+    Plan pl;
+};
+
+gdg_status gdg_plan_create(int op, const gdg_args* args, const int32_t* offs, int E, int N, int K,
+                           gdg_dtype out_dtype, int accumulate, gdg_plan** plan) {
+    if (!plan) return GDG_EINVAL;
+    *plan = nullptr;
+    gdg_plan* h = new (std::nothrow) gdg_plan;
+    if (!h) return GDG_EINVAL;
+    const gdg_status st = make_plan(op, args, offs, E, N, K, out_dtype, accumulate, &h->pl);
+    if (st != GDG_OK) {
+        delete h;
+        return st;
+    }
+    *plan = h;
+    return GDG_OK;
+}
+
+gdg_status gdg_plan_launch(const gdg_plan* plan, void* stream) {
+    if (!plan) return GDG_EINVAL;
+    return launch_plan(plan->pl, static_cast<cudaStream_t>(stream));
+}
+
+void gdg_plan_destroy(gdg_plan* plan) { delete plan; }
 
 const char* gdg_status_string(gdg_status status) {
     switch (status) {

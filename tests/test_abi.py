@@ -127,3 +127,30 @@ def test_status_strings(lib):
     for s in range(7):
         assert lib.gdg_status_string(s)
     assert b"unknown" in lib.gdg_status_string(99)
+
+
+def test_plan_refusals_leave_no_plan(lib):
+    """gdg_plan_create runs the entry points' checks on the host and binds nothing on failure."""
+    lib.gdg_plan_create.restype = ctypes.c_int
+    lib.gdg_plan_create.argtypes = [ctypes.c_int, ctypes.POINTER(Args), ctypes.c_void_p,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.POINTER(ctypes.c_void_p)]
+    lib.gdg_plan_launch.restype = ctypes.c_int
+    lib.gdg_plan_launch.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.gdg_plan_destroy.restype = None
+    lib.gdg_plan_destroy.argtypes = [ctypes.c_void_p]
+    h = ctypes.c_void_p(1)
+    # (op, E, out dtype, accumulate): fp32 fwd, accumulating dgrad, accumulate=2, unknown op,
+    # no groups
+    for op, E, dtype, acc in ((0, 4, 1, 0), (1, 4, 0, 1), (2, 4, 0, 2), (3, 4, 0, 0), (0, 0, 0, 0)):
+        assert lib.gdg_plan_create(op, ctypes.byref(good()), OFFS, E, 256, 256, dtype, acc,
+                                   ctypes.byref(h)) == EINVAL
+        assert h.value is None
+    assert lib.gdg_plan_create(0, ctypes.byref(good()), OFFS, 4, 128, 256, 0, 0,
+                               ctypes.byref(h)) == EALIGN
+    assert lib.gdg_plan_create(2, ctypes.byref(good(split=64)), OFFS, 4, 256, 256, 0, 0,
+                               ctypes.byref(h)) == EWORKSPACE
+    assert h.value is None
+    assert lib.gdg_plan_create(0, ctypes.byref(good()), OFFS, 4, 256, 256, 0, 0, None) == EINVAL
+    assert lib.gdg_plan_launch(None, None) == EINVAL
+    lib.gdg_plan_destroy(None)
