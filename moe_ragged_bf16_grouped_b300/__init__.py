@@ -27,7 +27,7 @@ __all__ = [
     "grouped_det_gemm_workspace_bytes", "grouped_det_gemm_auto_split_rows",
     "grouped_det_gemm_wgrad_noalloc", "GDG_NOALLOC_SCRATCH_BYTES", "GroupedDetGemmPlan",
     "prepare_grouped_det_gemm_fwd", "prepare_grouped_det_gemm_dgrad",
-    "prepare_grouped_det_gemm_wgrad",
+    "prepare_grouped_det_gemm_wgrad", "grouped_det_mm", "GroupedDetMm",
     "gdg_status_string", "gdg_device_error", "library_path",
 ]
 
@@ -335,3 +335,6 @@ def grouped_det_gemm_wgrad_noalloc(g: torch.Tensor, x: torch.Tensor, offs: torch
     _call(_lib.grouped_det_gemm_wgrad_noalloc, "grouped_det_gemm_wgrad_noalloc", args, offs, E,
           N, K, _dtype_code(out.dtype), int(accumulate), _stream_ptr(stream, g.device))
     return out
+
+
+from .autograd import GroupedDetMm, grouped_det_mm  # noqa: E402  (needs the functions above)

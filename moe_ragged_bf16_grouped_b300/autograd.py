@@ -1,0 +1,97 @@
+"""Autograd over the C ABI: ``grouped_det_mm(x, w, offs, *, fuse_wgrad_accumulation=False)``.
+
+The computation table of the "Cake ragged BF16 grouped GEMM (experimental)" docs page, wired for
+training: the forward is ``grouped_det_gemm_fwd`` (Y[g] = X[g] @ W[e].T), the backward runs
+``grouped_det_gemm_dgrad`` for x and ``grouped_det_gemm_wgrad`` for w.  Every step is one of the
+library's kernels; this module only routes tensors.
+
+``fuse_wgrad_accumulation=True`` follows the Megatron / Transformer Engine ``main_grad``
+convention that the MoE grouped GEMM pull request adopts for the deterministic wrapper
+(section "Deterministic weight-gradient accumulation"):
+
+- ``w.main_grad`` (fp32 or bf16, w's shape and device; here also contiguous) is checked when the
+  forward runs and read again by the backward;
+- the backward adds the deterministic dW into it with the fused accumulate (the bits of
+  ``main_grad.add_(dW)``), every time it runs: ``retain_graph`` and a second backward add twice,
+  and so does ``torch.autograd.grad`` whose inputs exclude w;
+- it then returns a fresh placeholder gradient for w when w has the attribute
+  ``grad_added_to_main_grad`` (which it sets to True; zeros when ``w.zero_out_wgrad`` is true,
+  else uninitialised), and None otherwise;
+- ``create_graph`` (a differentiable backward), ``torch.jit.trace`` and ``torch.compile`` raise
+  NotImplementedError.
+
+Without fusion, w's gradient is dW in w's dtype (bf16).  Reentrant activation checkpointing is
+not detected (the pages refuse it); non-reentrant checkpointing works like any autograd graph.
+"""
+from __future__ import annotations
+
+import sys
+
+import torch
+
+_gdg = sys.modules[__package__]
+
+
+def _check_main_grad(w: torch.Tensor) -> torch.Tensor:
+    mg = getattr(w, "main_grad", None)
+    if mg is None:
+        raise ValueError("fuse_wgrad_accumulation=True needs w.main_grad")
+    if mg.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"w.main_grad must be float32 or bfloat16, got {mg.dtype}")
+    if tuple(mg.shape) != tuple(w.shape) or mg.device != w.device:
+        raise ValueError("w.main_grad must have w's shape and device")
+    if not mg.is_contiguous():
+        raise ValueError("w.main_grad must be contiguous")
+    return mg
+
+
+def _refuse_tracing():
+    if torch.jit.is_tracing() or torch.compiler.is_compiling():
+        raise NotImplementedError("grouped_det_mm cannot be traced or compiled")
+
+
+class GroupedDetMm(torch.autograd.Function):
+    """Y = grouped fwd(x, w, offs); backward: dgrad for x, wgrad (or fused main_grad
+    accumulation) for w.  Inputs are bf16 and contiguous; offs is int32 on the same device."""
+
+    @staticmethod
+    def forward(ctx, x, w, offs, fuse_wgrad_accumulation=False):
+        if not isinstance(fuse_wgrad_accumulation, bool):
+            raise ValueError("fuse_wgrad_accumulation must be a bool")
+        _refuse_tracing()
+        if fuse_wgrad_accumulation:
+            _check_main_grad(w)
+        y = _gdg.grouped_det_gemm_fwd(x, w, offs)
+        ctx.save_for_backward(x, w, offs)
+        ctx.fuse = fuse_wgrad_accumulation
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        if torch.is_grad_enabled():
+            raise NotImplementedError("grouped_det_mm does not support create_graph")
+        x, w, offs = ctx.saved_tensors
+        dy = dy.contiguous()
+        dx = dw = None
+        if ctx.needs_input_grad[0]:
+            dx = _gdg.grouped_det_gemm_dgrad(dy, w, offs)
+        if ctx.needs_input_grad[1]:
+            if ctx.fuse:
+                mg = _check_main_grad(w)
+                _gdg.grouped_det_gemm_wgrad(dy, x, offs, out=mg, accumulate=True)
+                if hasattr(w, "grad_added_to_main_grad"):
+                    w.grad_added_to_main_grad = True
+                    if getattr(w, "zero_out_wgrad", False):
+                        dw = torch.zeros(w.shape, dtype=w.dtype, device=w.device)
+                    else:
+                        dw = torch.empty(w.shape, dtype=w.dtype, device=w.device)
+            else:
+                dw = _gdg.grouped_det_gemm_wgrad(dy, x, offs, out_dtype=w.dtype)
+        return dx, dw, None, None
+
+
+def grouped_det_mm(x: torch.Tensor, w: torch.Tensor, offs: torch.Tensor, *,
+                   fuse_wgrad_accumulation: bool = False) -> torch.Tensor:
+    """Ragged grouped matmul Y[g] = X[g] @ W[e].T with deterministic gradients (offs: int32
+    cumulative ends of the groups)."""
+    return GroupedDetMm.apply(x, w, offs, fuse_wgrad_accumulation)

@@ -139,7 +139,12 @@ cudaError_t set_up_kernel(int sms, int* pairs) {
 // Per-device set-up, once: SM count, device error word address, kernel attributes.
 DeviceInfo* device_info(gdg_status* st) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    // cudaSetDevice binds the device's primary context to this thread: the tensor-map encoder
+    // is a driver-API call and needs a current context, which a thread that has made no
+    // runtime call yet (an autograd worker thread, say) does not have.
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices ||
+        cudaSetDevice(dev) != cudaSuccess) {
+        cudaGetLastError();
         *st = GDG_ECUDA;
         return nullptr;
     }
@@ -398,6 +403,9 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
 
 gdg_status launch_plan(const Plan& pl, cudaStream_t s) {
     if (!pl.launch) return GDG_OK;
+    // The launch status is read from this host thread's last-error slot: clear what an earlier,
+    // unrelated call on the thread may have left there (a sticky error survives and is seen).
+    cudaGetLastError();
     const GemmParams& p = pl.p;
     const int g = pl.grid;
     if (pl.op == GDG_OP_FWD) {
