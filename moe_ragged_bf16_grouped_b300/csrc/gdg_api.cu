@@ -83,6 +83,14 @@ bool encode_row_blocks(CUtensorMap* m, const void* base, int64_t rows, int cols,
     return encode(m, base, 3, dims, strides, box);
 }
 
+// [rows, cols] bf16 as a plain 2-D map with box {64, box_rows} (wgrad tail steps).
+bool encode_rows_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, uint32_t box_rows) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(cols) * 2};
+    const uint32_t box[2] = {64, box_rows};
+    return encode(m, base, 2, dims, strides, box);
+}
+
 // W [E, N, K] seen as {64 k, N, K/64 blocks, E}: box {64, 128, 2, 1} brings two 64-wide k
 // blocks of 128 n-rows of one expert (fwd: 128 n x 128 k; dgrad: 128 k x 128 n).
 bool encode_weight_blocks(CUtensorMap* m, const void* base, int E, int N, int K) {
@@ -359,7 +367,9 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
     const void* a = rows > 0 ? args->a : args->out;
     const void* b = rows > 0 ? args->b : args->out;
     if (!encode_row_blocks(&p.tmA, a, map_rows, N, 128u) ||
-        !encode_row_blocks(&p.tmB[0], b, map_rows, K, 128u))
+        !encode_row_blocks(&p.tmB[0], b, map_rows, K, 128u) ||
+        !encode_rows_2d(&p.tmTail[0], a, map_rows, N, 16u) ||
+        !encode_rows_2d(&p.tmTail[1], b, map_rows, K, 16u))
         return GDG_ECUDA;
     if (!split && accumulate &&
         !encode_prefetch(&p.tmPre, args->out, static_cast<int64_t>(E) * N, K,

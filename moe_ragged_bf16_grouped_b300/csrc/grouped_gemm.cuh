@@ -70,8 +70,11 @@ struct Ring {
 };
 constexpr int kSubBytes = 128 * 128;        // one 128-row block of 64 bf16 (128 B) per row
 constexpr int kEpiWarps = 8;
-constexpr int kEpiBoxBytes = 32 * 128;      // wgrad staging box per warp: 32 rows x 128 B
+constexpr int kEpiBoxBytes = 32 * 64;       // wgrad staging box per warp: 32 rows x 64 B
 constexpr int kEpiBytes = kEpiWarps * kEpiBoxBytes;
+constexpr int kTailSub = 16 * 128;          // wgrad tail step: one 64-column block, 16 rows
+constexpr int kTailBytes = 4 * kTailSub;    // G blocks 0, 1 then X blocks 0, 1 of this CTA
+constexpr int kTailBufs = 2;
 constexpr int kThreads = 384;               // GEMM kernel: 4 role warps + 8 epilogue warps
 constexpr int kReduceThreads = 256;
 constexpr int kMaxE = 1024;
@@ -93,6 +96,7 @@ struct GemmParams {
     CUtensorMap tmB[5];     // fwd: X {k%64, row, k/64}, dgrad: G {n%64, row, n/64},
                             // box{64, 8<<i, 2}; wgrad: tmB[0] = X {k%64, row, k/64} box{64,128,2}
     CUtensorMap tmPre;      // wgrad accumulate: out as {K, E*N}, box {256, 128} (L2 prefetch)
+    CUtensorMap tmTail[2];  // wgrad tail steps: G {N, rows}, X {K, rows}, box {64, 16}
     const int32_t* offs;
     void* out;
     float* partial;         // wgrad split form: [max_units][256][256] fp32
@@ -105,10 +109,11 @@ struct GemmParams {
 };
 
 struct SmemCtl {
-    uint64_t full[kMaxStages];  // even CTA: both CTAs' copies of a stage have landed (a wgrad
-                                // tail stage: both CTAs' fixers have zeroed its tail rows)
+    uint64_t full[kMaxStages];  // even CTA: both CTAs' copies of a stage have landed
     uint64_t empty[kMaxStages]; // both CTAs: the pair's MMAs have read the stage
-    uint64_t tail_full[kMaxStages];   // both CTAs (wgrad): this CTA's copies of a tail stage
+    uint64_t tb_full[kTailBufs];    // both CTAs (wgrad): this CTA's tail step has landed
+    uint64_t tb_fixed[kTailBufs];   // even CTA: both CTAs zeroed the tail step's extra rows
+    uint64_t tb_empty[kTailBufs];   // both CTAs: the pair's MMA has read the tail step
     uint64_t tfull[2];          // both CTAs: the accumulator is complete
     uint64_t tempty[2];         // even CTA: all 16 epilogue warps of the pair drained it
     uint64_t drain;
@@ -119,7 +124,7 @@ struct SmemCtl {
 };
 
 constexpr size_t kGemmSmemBytes =
-    1024 + static_cast<size_t>(kRingBytes) + kEpiBytes + sizeof(SmemCtl);
+    1024 + static_cast<size_t>(kRingBytes) + kEpiBytes + kTailBufs * kTailBytes + sizeof(SmemCtl);
 
 // ------------------------------------------------------------------ schedule
 
@@ -285,9 +290,16 @@ __device__ __forceinline__ int chunks_of(int nkb) {
     return (nkb + kChunkStages - 1) / kChunkStages;
 }
 
-// wgrad: a stage whose rows end inside a 16-row MMA step (rows of another group or split
-// follow in that step) must have those rows zeroed before the MMAs read it.
-__device__ __forceinline__ bool needs_fix(int valid) { return valid < kBK && (valid & 15) != 0; }
+// wgrad: a unit whose rows end inside a 16-row MMA step (rows of another group or split
+// follow in that step).  Its last ring stage serves only the whole 16-row steps; the partial
+// step is loaded on its own into a tail buffer, one unit ahead, where both CTAs zero the rows
+// past the unit's end before the MMA reads it.  Returns the rows of the last stage, or 0 when
+// the unit has no partial step.
+__device__ __forceinline__ int tail_rows(int nred, int nkb) {
+    if (nkb <= 0) return 0;
+    const int v = nred - (nkb - 1) * kBK;
+    return (v & 15) != 0 ? v : 0;
+}
 
 
 struct Tile {
@@ -425,7 +437,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     using R = Ring<RT>;
     uint8_t* stage_area = smem + kRingBytes;                 // wgrad epilogue staging boxes
-    SmemCtl* c = reinterpret_cast<SmemCtl*>(stage_area + kEpiBytes);
+    uint8_t* tail_area = stage_area + kEpiBytes;              // wgrad tail-step buffers
+    SmemCtl* c = reinterpret_cast<SmemCtl*>(tail_area + kTailBufs * kTailBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Shape sh = unit_shape<OP>(p);
@@ -437,11 +450,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < R::kStages; ++s) {
-            // wgrad: a stage is released by two arrivals, the even producer's two (plain
-            // stage) or one per CTA's fixer (tail stage).
-            mbar_init(&c->full[s], OP == OP_WGRAD ? 2 : 1);
+            mbar_init(&c->full[s], 1);
             mbar_init(&c->empty[s], 1);
-            mbar_init(&c->tail_full[s], 1);
+        }
+        for (int b = 0; b < kTailBufs; ++b) {
+            mbar_init(&c->tb_full[b], 1);
+            mbar_init(&c->tb_fixed[b], 2);   // one arrival per CTA's fixer
+            mbar_init(&c->tb_empty[b], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&c->tfull[b], 1);
@@ -477,8 +492,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- TMA producer (both CTAs)
         if (lane == 0) {
             const uint32_t full0 = mapa_shared(smem_u32(&c->full[0]), 0u);
-            const uint32_t tail0 = mapa_shared(smem_u32(&c->tail_full[0]), pr.rank);
-            int stage = 0;
+            int stage = 0, jt = 0;   // jt: units with a tail step so far
             uint32_t phase = 0;
             bool ok = true;
             for (int u = pair; u < total && ok; u += npairs) {
@@ -493,20 +507,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // The epilogue reads this CTA's 128 x 256 block of out after the unit's
                     // mainloop: start bringing it into L2 now.
                     tma_prefetch_2d(&p.tmPre, t.c0, t.e * p.N + fa);
+                if (OP == OP_WGRAD) {
+                    const int v = tail_rows(t.nred, t.nkb);
+                    if (v) {
+                        // The unit's partial 16-row step, into its tail buffer (own barrier),
+                        // ahead of the unit's ring stages.
+                        const int tb = jt & 1;
+                        if (!wait_bar(&c->tb_empty[tb], ((jt >> 1) & 1) ^ 1u, c, pr, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        const int rt0 = t.r0 + (t.nkb - 1) * kBK + (v & ~15);
+                        const int xb = (t.c0 + (kBN / 2) * static_cast<int>(pr.rank));
+                        uint8_t* tbuf = tail_area + tb * kTailBytes;
+                        mbar_arrive_expect_tx(&c->tb_full[tb], kTailBytes);
+                        tma_load_2d(tbuf, &p.tmTail[0], &c->tb_full[tb], fa, rt0);
+                        tma_load_2d(tbuf + kTailSub, &p.tmTail[0], &c->tb_full[tb], fa + 64, rt0);
+                        tma_load_2d(tbuf + 2 * kTailSub, &p.tmTail[1], &c->tb_full[tb], xb, rt0);
+                        tma_load_2d(tbuf + 3 * kTailSub, &p.tmTail[1], &c->tb_full[tb], xb + 64, rt0);
+                        ++jt;
+                    }
+                }
                 for (int kb = 0; kb < t.nkb; ++kb) {
                     if (!wait_bar(&c->empty[stage], phase ^ 1u, c, pr, p.err)) { ok = false; break; }
                     uint8_t* a = smem + stage * R::kStageBytes;
                     uint8_t* b = a + kABytes;
-                    uint32_t fb = full0 + stage * 8u;
-                    if (OP == OP_WGRAD && needs_fix(t.nred - kb * kBK)) {
-                        // Tail stage: this CTA's copies complete on its own barrier; its fixer
-                        // zeroes the rows past the group end, then releases the stage.
-                        fb = tail0 + stage * 8u;
-                        mbar_arrive_expect_tx(&c->tail_full[stage], kABytes + R::kBBytes);
-                    } else if (even) {
-                        mbar_arrive_expect_tx(&c->full[stage], bytes);
-                        if (OP == OP_WGRAD) mbar_arrive(&c->full[stage]);
-                    }
+                    const uint32_t fb = full0 + stage * 8u;
+                    if (even) mbar_arrive_expect_tx(&c->full[stage], bytes);
                     // One copy per operand and stage: each map's third dimension walks
                     // 64-column blocks, so two blocks land as consecutive sub-tiles (a block
                     // past the tensor's extent reads as zeros).
@@ -542,7 +569,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // handed to the epilogue (its tfull / tempty phase).  A chunked unit keeps buffer A
         // for its chunks and hands buffer B to the epilogue for the running sum.
         if (even && lane == 0) {
-            int stage = 0, nextb = 0;
+            int stage = 0, nextb = 0, jt = 0;   // jt: units with a tail step so far
             uint32_t phase = 0;
             Acq acq;
             bool ok = true;
@@ -567,6 +594,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // the two 64-wide M/N blocks are kSubBytes apart (LBO).
                 const uint32_t b_sub = static_cast<uint32_t>((8 << bi) * 128);
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(A * kBN);
+                const int tv = (OP == OP_WGRAD) ? tail_rows(t.nred, t.nkb) : 0;
                 for (int ch = 0; ch < nch && ok; ++ch) {
                     if (!wait_bar(&c->tempty[A], (acq.of(A) & 1u) ^ 1u, c, pr, p.err)) { ok = false; break; }
                     tc_fence_after();
@@ -579,8 +607,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const uint32_t b_addr = a_addr + kABytes;
                         const int valid = t.nred - kb * kBK;
                         // fwd / dgrad: a last stage of 64 (K or N is a multiple of 64) skips
-                        // the zero-filled second block.
-                        const int nsteps = valid < kBK ? (valid + 15) >> 4 : kBK / 16;
+                        // the zero-filled second block.  wgrad: a last stage with a partial
+                        // step serves only its whole 16-row steps; the partial one comes from
+                        // the tail buffer below.
+                        const bool tstep = tv != 0 && kb == t.nkb - 1;
+                        const int nsteps = tstep ? (valid >> 4)
+                                                 : (valid < kBK ? (valid + 15) >> 4 : kBK / 16);
                         for (int kk = 0; kk < nsteps; ++kk) {
                             const uint32_t kblk = static_cast<uint32_t>(kk >> 2), k16 = kk & 3;
                             const uint64_t ad =
@@ -595,6 +627,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                         umma_commit_pair(&c->empty[stage], 3);
                         if (++stage == R::kStages) { stage = 0; phase ^= 1u; }
+                        if (tstep) {
+                            const int tb = jt & 1;
+                            if (!wait_bar(&c->tb_fixed[tb], (jt >> 1) & 1, c, pr, p.err)) { ok = false; break; }
+                            tc_fence_after();
+                            // G blocks and X blocks: 16 rows x 128 B each, the two 64-wide blocks
+                            // of an operand kTailSub apart (LBO).
+                            const uint32_t ta = smem_u32(tail_area + tb * kTailBytes);
+                            umma_bf16_pair(d_tmem, sdesc_sw128(ta, kTailSub, 1024),
+                                           sdesc_sw128(ta + 2 * kTailSub, kTailSub, 1024), idesc,
+                                           (kb != kb0 || nsteps != 0) ? 1u : 0u);
+                            umma_commit_pair(&c->tb_empty[tb], 3);
+                            ++jt;
+                        }
                     }
                     if (!ok) break;
                     // Arrives once this chunk's MMAs (if any: an empty group has none) are done.
@@ -610,52 +655,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 3) {
         // ---------------------------------------------------------- wgrad tail fixer (both CTAs)
+        // Zeroes the rows past the unit's end in this CTA's copy of each tail step, then tells
+        // the even CTA's MMA.
         if (OP == OP_WGRAD) {
-            const uint32_t full0 = mapa_shared(smem_u32(&c->full[0]), 0u);
-            int stage = 0;
-            uint32_t tphase = 0;     // per stage: parity of the next tail_full phase
-            bool ok = true;
-            for (int u = pair; u < total && ok; u += npairs) {
+            int jt = 0;
+            for (int u = pair; u < total; u += npairs) {
                 const Tile t = decode_unit<OP, RT>(p, cu, sh, u);
-                for (int kb = 0; kb < t.nkb; ++kb) {
-                    const int valid = t.nred - kb * kBK;
-                    if (needs_fix(valid)) {
-                        if (!wait_bar_warp(&c->tail_full[stage], (tphase >> stage) & 1u, c, pr,
-                                           p.err)) {
-                            ok = false;
-                            break;
-                        }
-                        tphase ^= 1u << stage;
-                        // Rows [valid, round_up(valid, 16)) of this CTA's four sub-tiles (A and
-                        // B, two 64-wide blocks each) hold rows of another group or another
-                        // split: zero them.  A whole 128-byte row is zeroed, so the swizzle of
-                        // its 16-byte chunks does not matter.
-                        // Lane l zeroes 16-byte chunk l % 8 of rows valid + l / 8, +4, ...
-                        const int zend = (valid + 15) & ~15;
-                        uint8_t* base = smem + stage * R::kStageBytes + (lane & 7) * 16;
+                const int v = tail_rows(t.nred, t.nkb);
+                if (!v) continue;
+                const int tb = jt & 1;
+                if (!wait_bar_warp(&c->tb_full[tb], (jt >> 1) & 1, c, pr, p.err)) break;
+                // Rows [v % 16, 16) of the four 16-row blocks; lane l zeroes 16-byte chunk l % 8
+                // of rows v % 16 + l / 8, + 4, ...  A whole 128-byte row is zeroed, so the
+                // swizzle of its chunks does not matter.
+                uint8_t* base = tail_area + tb * kTailBytes + (lane & 7) * 16;
 #pragma unroll
-                        for (int bx = 0; bx < 4; ++bx)
-                            for (int r = valid + (lane >> 3); r < zend; r += 4)
-                                *reinterpret_cast<uint4*>(base + bx * kSubBytes + r * 128) =
-                                    make_uint4(0, 0, 0, 0);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            if (even) mbar_arrive(&c->full[stage]);
-                            else mbar_arrive_cluster(full0 + stage * 8u);
-                        }
-                        __syncwarp();
-                    }
-                    if (++stage == R::kStages) stage = 0;
+                for (int bx = 0; bx < 4; ++bx)
+                    for (int r = (v & 15) + (lane >> 3); r < 16; r += 4)
+                        *reinterpret_cast<uint4*>(base + bx * kTailSub + r * 128) = make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (even) mbar_arrive(&c->tb_fixed[tb]);
+                    else mbar_arrive_cluster(mapa_shared(smem_u32(&c->tb_fixed[tb]), 0u));
                 }
+                ++jt;
             }
         }
     } else if (warp >= 4 && OP == OP_WGRAD) {
         // ---------------------------------------------------------- wgrad epilogue (both CTAs)
         // Each warp writes 32 dW rows (its TMEM lanes) x 128 columns (one half of the tile) in
-        // boxes of 32 rows x 128 bytes (64 bf16 or 32 fp32 columns): TMEM -> registers (one
-        // row per thread) -> shared memory (128-byte swizzle) -> registers in line order (8
-        // threads per 128-byte line) -> coalesced global stores.  With accumulate the old
+        // boxes of 32 rows x 64 bytes (32 bf16 or 16 fp32 columns): TMEM -> registers (one row
+        // per thread) -> shared memory (64-byte swizzle) -> registers in line order (4 threads
+        // per 64-byte row piece) -> coalesced global stores.  With accumulate the old
         // values are loaded in the same line order (after an L2 prefetch of the block issued
         // when the unit's loads started) and added there.
         const int q = warp & 3, ew = warp - 4;          // TMEM lanes [32q, 32q + 32)
@@ -666,10 +698,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         constexpr bool acc = EPI == EPI_FP32_ACC || EPI == EPI_BF16_ACC;
         constexpr bool f32 = EPI == EPI_FP32 || EPI == EPI_FP32_ACC || EPI == EPI_PARTIAL;
         constexpr int osz = f32 ? 4 : 2;
-        constexpr int box_cols = f32 ? 32 : 64;
-        const int rr = lane >> 3, gg = lane & 7;        // line-order phase: rows rr + 4j, chunk gg
-        uint8_t* wslot = box + lane * 128;              // this lane's row in the write phase
-        const int wsw = lane & 7;
+        const int rr = lane >> 2, gg = lane & 3;        // line-order phase: rows rr + 8j, chunk gg
+        uint8_t* wslot = box + lane * 64;               // this lane's row in the write phase
+        const int wsw = (lane >> 1) & 3;                // 64-byte swizzle: chunk g at g ^ wsw
         bool ok = true;
         int nextb = 0;
         Acq acq;                        // the MMA issuer's buffer plan, followed step by step
@@ -729,70 +760,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         (static_cast<size_t>(t.e) * p.N + t.f0 + mrow0) * ldo +
                         static_cast<size_t>(t.c0) * osz;
             }
-            for (int cb = 128 * hc; cb < cend; cb += box_cols) {
-                uint8_t* gline = obase + static_cast<size_t>(rr) * ldo + cb * osz + gg * 16;
-                uint4 old[8];
-                if constexpr (acc) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        old[j] = *reinterpret_cast<const uint4*>(gline + 4 * j * ldo);
-                }
-                // The box's row for this thread as 8 chunks of 16 bytes (32 words).
-                uint32_t pk[32];
-                if constexpr (f32) {
-                    if (t.nkb > 0) {
-                        tmem_ld_32x32b_x32(taddr + cb, pk);
-                        tmem_ld_wait();
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) pk[j] = 0u;   // +0.0f: empty group
-                    }
+            // 32 TMEM columns at a time: one box of 32 bf16 columns, or two boxes of 16 fp32.
+            for (int cb = 128 * hc; cb < cend; cb += 32) {
+                uint32_t r[32];
+                if (t.nkb > 0) {
+                    tmem_ld_32x32b_x32(taddr + cb, r);
+                    tmem_ld_wait();
                 } else {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t r[32];
-                        if (t.nkb > 0) {
-                            tmem_ld_32x32b_x32(taddr + cb + 32 * h, r);
-                            tmem_ld_wait();
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) r[j] = 0u;
-                        }
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            pk[16 * h + j] = pack_bf16x2(__uint_as_float(r[2 * j]),
-                                                         __uint_as_float(r[2 * j + 1]));
-                    }
+                    for (int j = 0; j < 32; ++j) r[j] = 0u;   // +0.0f: empty group
                 }
-                // One row per thread: 16-byte chunk g of row `lane` goes to slot g ^ (lane & 7).
 #pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    *reinterpret_cast<uint4*>(wslot + ((g ^ wsw) << 4)) =
-                        make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-                __syncwarp();
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int row = rr + 4 * j;
-                    uint4 v = *reinterpret_cast<const uint4*>(box + row * 128 + ((gg ^ (row & 7)) << 4));
+                for (int h = 0; h < (f32 ? 2 : 1); ++h) {
+                    const int c0 = cb + 16 * h;              // first column of the box
+                    uint8_t* gline = obase + static_cast<size_t>(rr) * ldo + c0 * osz + gg * 16;
+                    uint4 old[4];
                     if constexpr (acc) {
-                        const uint4 o = old[j];
-                        if constexpr (f32) {
-                            // out = RN32(out + dW): fp32 out.add_(dW)
-                            v = make_uint4(__float_as_uint(__fadd_rn(__uint_as_float(o.x), __uint_as_float(v.x))),
-                                           __float_as_uint(__fadd_rn(__uint_as_float(o.y), __uint_as_float(v.y))),
-                                           __float_as_uint(__fadd_rn(__uint_as_float(o.z), __uint_as_float(v.z))),
-                                           __float_as_uint(__fadd_rn(__uint_as_float(o.w), __uint_as_float(v.w))));
-                        } else {
-                            // out = bf16(float(out) + float(bf16(dW))): bf16 out.add_(dW)
-                            v.x = pack_bf16x2(__fadd_rn(bf16_lo(o.x), bf16_lo(v.x)), __fadd_rn(bf16_hi(o.x), bf16_hi(v.x)));
-                            v.y = pack_bf16x2(__fadd_rn(bf16_lo(o.y), bf16_lo(v.y)), __fadd_rn(bf16_hi(o.y), bf16_hi(v.y)));
-                            v.z = pack_bf16x2(__fadd_rn(bf16_lo(o.z), bf16_lo(v.z)), __fadd_rn(bf16_hi(o.z), bf16_hi(v.z)));
-                            v.w = pack_bf16x2(__fadd_rn(bf16_lo(o.w), bf16_lo(v.w)), __fadd_rn(bf16_hi(o.w), bf16_hi(v.w)));
-                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            old[j] = *reinterpret_cast<const uint4*>(gline + 8 * j * ldo);
                     }
-                    *reinterpret_cast<uint4*>(gline + 4 * j * ldo) = v;
+                    // One row per thread, four 16-byte chunks.
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        uint4 v;
+                        if constexpr (f32) {
+                            const uint32_t* w = r + 16 * h + 4 * g;
+                            v = make_uint4(w[0], w[1], w[2], w[3]);
+                        } else {
+                            const uint32_t* w = r + 8 * g;
+                            v = make_uint4(pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                                           pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                                           pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                                           pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
+                        }
+                        *reinterpret_cast<uint4*>(wslot + ((g ^ wsw) << 4)) = v;
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int row = rr + 8 * j;
+                        uint4 v = *reinterpret_cast<const uint4*>(box + row * 64 +
+                                                                  ((gg ^ ((row >> 1) & 3)) << 4));
+                        if constexpr (acc) {
+                            const uint4 o = old[j];
+                            if constexpr (f32) {
+                                // out = RN32(out + dW): fp32 out.add_(dW)
+                                v = make_uint4(__float_as_uint(__fadd_rn(__uint_as_float(o.x), __uint_as_float(v.x))),
+                                               __float_as_uint(__fadd_rn(__uint_as_float(o.y), __uint_as_float(v.y))),
+                                               __float_as_uint(__fadd_rn(__uint_as_float(o.z), __uint_as_float(v.z))),
+                                               __float_as_uint(__fadd_rn(__uint_as_float(o.w), __uint_as_float(v.w))));
+                            } else {
+                                // out = bf16(float(out) + float(bf16(dW))): bf16 out.add_(dW)
+                                v.x = pack_bf16x2(__fadd_rn(bf16_lo(o.x), bf16_lo(v.x)), __fadd_rn(bf16_hi(o.x), bf16_hi(v.x)));
+                                v.y = pack_bf16x2(__fadd_rn(bf16_lo(o.y), bf16_lo(v.y)), __fadd_rn(bf16_hi(o.y), bf16_hi(v.y)));
+                                v.z = pack_bf16x2(__fadd_rn(bf16_lo(o.z), bf16_lo(v.z)), __fadd_rn(bf16_hi(o.z), bf16_hi(v.z)));
+                                v.w = pack_bf16x2(__fadd_rn(bf16_lo(o.w), bf16_lo(v.w)), __fadd_rn(bf16_hi(o.w), bf16_hi(v.w)));
+                            }
+                        }
+                        *reinterpret_cast<uint4*>(gline + 8 * j * ldo) = v;
+                    }
+                    __syncwarp();   // the box is rewritten by the next box
                 }
-                __syncwarp();   // the box is rewritten by the next iteration
             }
             tc_fence_before();
             __syncwarp();
