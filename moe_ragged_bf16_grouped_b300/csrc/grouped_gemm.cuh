@@ -710,6 +710,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int A = nextb, B = nextb ^ 1;
             const uint32_t lanebase = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
             const int cend = min(128 * hc + 128, t.ncols);
+            uint8_t* obase;
+            size_t ldo;
+            if (EPI == EPI_PARTIAL) {
+                obase = reinterpret_cast<uint8_t*>(p.partial) +
+                        (static_cast<size_t>(t.u) * kPairM + mrow0) * kBN * 4;
+                ldo = static_cast<size_t>(kBN) * 4;
+            } else {
+                ldo = static_cast<size_t>(p.K) * osz;
+                obase = reinterpret_cast<uint8_t*>(p.out) +
+                        (static_cast<size_t>(t.e) * p.N + t.f0 + mrow0) * ldo +
+                        static_cast<size_t>(t.c0) * osz;
+            }
+            // This warp's 64 or 128 columns as boxes of 32 rows x 64 bytes (16 fp32 or 32
+            // bf16 columns; K % 64 == 0, so a warp has 0, 2 or 4 bf16 / 0, 4 or 8 fp32 boxes).
+            // Box b is bytes [64 b, 64 b + 64) of the warp's row segments.  With accumulate,
+            // the old values of the next kAhead boxes are always in flight.
+            constexpr int kBoxCols = f32 ? 16 : 32;
+            constexpr int kPer = 32 / kBoxCols;             // boxes per 32 TMEM columns
+            constexpr int kBoxes = 128 / kBoxCols;
+            constexpr int kAhead = acc ? 3 : 1;
+            const int nbox = max(0, cend - 128 * hc) / kBoxCols;
+            uint8_t* gseg = obase + static_cast<size_t>(rr) * ldo + (128 * hc) * osz + gg * 16;
+            uint4 old[kAhead][4];
+            auto first_loads = [&]() {
+                if constexpr (acc) {
+#pragma unroll
+                    for (int b = 0; b < kAhead; ++b)
+                        if (b < nbox)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                old[b][j] = *reinterpret_cast<const uint4*>(gseg + b * 64 + 8 * j * ldo);
+                }
+            };
             int fb = A;                 // the buffer that ends up holding the unit's value
             if (nch > 1) {
                 // Chunked unit: B receives chunk 0, then B = RN(B + chunk c) for c = 1, 2, ...
@@ -742,92 +775,95 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 fb = B;
+                first_loads();
             } else {
+                first_loads();   // old values do not depend on this unit's MMAs
                 if (!wait_bar_warp(&c->tfull[A], acq.of(A) & 1u, c, pr, p.err)) { ok = false; break; }
                 tc_fence_after();
                 acq.bump(A);
             }
-            const uint32_t taddr = lanebase + static_cast<uint32_t>(fb * kBN);
-            uint8_t* obase;
-            size_t ldo;
-            if (EPI == EPI_PARTIAL) {
-                obase = reinterpret_cast<uint8_t*>(p.partial) +
-                        (static_cast<size_t>(t.u) * kPairM + mrow0) * kBN * 4;
-                ldo = static_cast<size_t>(kBN) * 4;
-            } else {
-                ldo = static_cast<size_t>(p.K) * osz;
-                obase = reinterpret_cast<uint8_t*>(p.out) +
-                        (static_cast<size_t>(t.e) * p.N + t.f0 + mrow0) * ldo +
-                        static_cast<size_t>(t.c0) * osz;
-            }
-            // 32 TMEM columns at a time: one box of 32 bf16 columns, or two boxes of 16 fp32.
-            for (int cb = 128 * hc; cb < cend; cb += 32) {
-                uint32_t r[32];
-                if (t.nkb > 0) {
-                    tmem_ld_32x32b_x32(taddr + cb, r);
-                    tmem_ld_wait();
-                } else {
+            const uint32_t taddr = lanebase + static_cast<uint32_t>(fb * kBN + 128 * hc);
+            uint32_t r[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = 0u;   // +0.0f: empty group
+            for (int b = 0; b < kBoxes; ++b) {
+                if (b >= nbox) break;
+                const int h = b % kPer;
+                if (h == 0) {
+                    if (t.nkb > 0) {
+                        tmem_ld_32x32b_x32(taddr + b * kBoxCols, r);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = 0u;   // +0.0f: empty group
+                    }
+                    if (b + kPer >= nbox) {
+                        // Every TMEM column of the unit is in registers: hand the buffer back
+                        // to the MMA before the remaining stores.
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (even) mbar_arrive(&c->tempty[fb]);
+                            else mbar_arrive_cluster_cta(tempty0 + fb * 8u);   // TMEM drained
+                        }
+                    }
                 }
+                // One row per thread, four 16-byte chunks.
 #pragma unroll
-                for (int h = 0; h < (f32 ? 2 : 1); ++h) {
-                    const int c0 = cb + 16 * h;              // first column of the box
-                    uint8_t* gline = obase + static_cast<size_t>(rr) * ldo + c0 * osz + gg * 16;
-                    uint4 old[4];
+                for (int g = 0; g < 4; ++g) {
+                    uint4 v;
+                    if constexpr (f32) {
+                        const uint32_t* w = r + 16 * h + 4 * g;
+                        v = make_uint4(w[0], w[1], w[2], w[3]);
+                    } else {
+                        const uint32_t* w = r + 8 * g;
+                        v = make_uint4(pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                                       pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                                       pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                                       pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
+                    }
+                    *reinterpret_cast<uint4*>(wslot + ((g ^ wsw) << 4)) = v;
+                }
+                __syncwarp();
+                uint8_t* gline = gseg + b * 64;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int row = rr + 8 * j;
+                    uint4 v = *reinterpret_cast<const uint4*>(box + row * 64 +
+                                                              ((gg ^ ((row >> 1) & 3)) << 4));
                     if constexpr (acc) {
+                        const uint4 o = old[b % kAhead][j];
+                        if constexpr (f32) {
+                            // out = RN32(out + dW): fp32 out.add_(dW)
+                            v = make_uint4(__float_as_uint(__fadd_rn(__uint_as_float(o.x), __uint_as_float(v.x))),
+                                           __float_as_uint(__fadd_rn(__uint_as_float(o.y), __uint_as_float(v.y))),
+                                           __float_as_uint(__fadd_rn(__uint_as_float(o.z), __uint_as_float(v.z))),
+                                           __float_as_uint(__fadd_rn(__uint_as_float(o.w), __uint_as_float(v.w))));
+                        } else {
+                            // out = bf16(float(out) + float(bf16(dW))): bf16 out.add_(dW)
+                            v.x = pack_bf16x2(__fadd_rn(bf16_lo(o.x), bf16_lo(v.x)), __fadd_rn(bf16_hi(o.x), bf16_hi(v.x)));
+                            v.y = pack_bf16x2(__fadd_rn(bf16_lo(o.y), bf16_lo(v.y)), __fadd_rn(bf16_hi(o.y), bf16_hi(v.y)));
+                            v.z = pack_bf16x2(__fadd_rn(bf16_lo(o.z), bf16_lo(v.z)), __fadd_rn(bf16_hi(o.z), bf16_hi(v.z)));
+                            v.w = pack_bf16x2(__fadd_rn(bf16_lo(o.w), bf16_lo(v.w)), __fadd_rn(bf16_hi(o.w), bf16_hi(v.w)));
+                        }
+                    }
+                    *reinterpret_cast<uint4*>(gline + 8 * j * ldo) = v;
+                }
+                if constexpr (acc) {
+                    if (b + kAhead < nbox)
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            old[j] = *reinterpret_cast<const uint4*>(gline + 8 * j * ldo);
-                    }
-                    // One row per thread, four 16-byte chunks.
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        uint4 v;
-                        if constexpr (f32) {
-                            const uint32_t* w = r + 16 * h + 4 * g;
-                            v = make_uint4(w[0], w[1], w[2], w[3]);
-                        } else {
-                            const uint32_t* w = r + 8 * g;
-                            v = make_uint4(pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
-                                           pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
-                                           pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
-                                           pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
-                        }
-                        *reinterpret_cast<uint4*>(wslot + ((g ^ wsw) << 4)) = v;
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int row = rr + 8 * j;
-                        uint4 v = *reinterpret_cast<const uint4*>(box + row * 64 +
-                                                                  ((gg ^ ((row >> 1) & 3)) << 4));
-                        if constexpr (acc) {
-                            const uint4 o = old[j];
-                            if constexpr (f32) {
-                                // out = RN32(out + dW): fp32 out.add_(dW)
-                                v = make_uint4(__float_as_uint(__fadd_rn(__uint_as_float(o.x), __uint_as_float(v.x))),
-                                               __float_as_uint(__fadd_rn(__uint_as_float(o.y), __uint_as_float(v.y))),
-                                               __float_as_uint(__fadd_rn(__uint_as_float(o.z), __uint_as_float(v.z))),
-                                               __float_as_uint(__fadd_rn(__uint_as_float(o.w), __uint_as_float(v.w))));
-                            } else {
-                                // out = bf16(float(out) + float(bf16(dW))): bf16 out.add_(dW)
-                                v.x = pack_bf16x2(__fadd_rn(bf16_lo(o.x), bf16_lo(v.x)), __fadd_rn(bf16_hi(o.x), bf16_hi(v.x)));
-                                v.y = pack_bf16x2(__fadd_rn(bf16_lo(o.y), bf16_lo(v.y)), __fadd_rn(bf16_hi(o.y), bf16_hi(v.y)));
-                                v.z = pack_bf16x2(__fadd_rn(bf16_lo(o.z), bf16_lo(v.z)), __fadd_rn(bf16_hi(o.z), bf16_hi(v.z)));
-                                v.w = pack_bf16x2(__fadd_rn(bf16_lo(o.w), bf16_lo(v.w)), __fadd_rn(bf16_hi(o.w), bf16_hi(v.w)));
-                            }
-                        }
-                        *reinterpret_cast<uint4*>(gline + 8 * j * ldo) = v;
-                    }
-                    __syncwarp();   // the box is rewritten by the next box
+                            old[b % kAhead][j] =
+                                *reinterpret_cast<const uint4*>(gseg + (b + kAhead) * 64 + 8 * j * ldo);
                 }
+                __syncwarp();   // the box is rewritten by the next box
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (even) mbar_arrive(&c->tempty[fb]);
-                else mbar_arrive_cluster_cta(tempty0 + fb * 8u);   // TMEM drained
+            if (nbox == 0) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (even) mbar_arrive(&c->tempty[fb]);
+                    else mbar_arrive_cluster_cta(tempty0 + fb * 8u);   // nothing to drain
+                }
             }
             if (nch == 1) nextb ^= 1;
         }
