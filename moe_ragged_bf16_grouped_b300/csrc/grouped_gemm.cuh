@@ -21,18 +21,18 @@
 // covered with 16-row granularity (N = round_up(rows in tile, 16)) instead of the
 // 128-row granularity of the M dimension; weights stream as the A operand.
 // For wgrad the reduction runs over the group's rows in 128-row stages starting exactly
-// at the group's first row.  A unit's last stage usually runs past the group end: its
-// copies complete on a barrier of their own CTA, a "fixer" warp in each CTA zeroes the
-// rows past the end in its own shared memory, and the two fixers' arrivals release the
-// stage to the MMA, which skips the steps past the last 16-row step.
+// at the group's first row.  A unit's last stage usually ends inside a 16-row MMA step: the
+// ring stage serves only the whole steps, and the partial step is copied on its own (16 rows
+// of each operand) into a small double-buffered tail buffer ahead of the unit's stages, where a
+// "fixer" warp in each CTA zeroes the rows past the unit's end before the MMA reads it.
 //
-// Warp roles (256 threads per CTA): warp 0 lane 0 issues TMA loads of this CTA's halves
-// into a kStages-deep ring, completing on the even CTA's "full" barriers; warp 1 lane 0 of
-// the even CTA issues the pair's MMAs into one of two TMEM accumulators (2 x 256 fp32
-// columns) and commits to the "empty" / "tmem full" barriers of both CTAs; warp 2 owns the
-// TMEM allocation; warp 3 of each CTA zeroes wgrad tail rows; warps 4..11 of both CTAs drain
-// their TMEM rows (tcgen05.ld; two warps per 32-lane quarter, one per half of the columns)
-// and write the outputs while the next tile's MMAs run into the other accumulator.
+// Warp roles (384 threads per CTA): warp 0 lane 0 issues TMA loads of this CTA's halves
+// into a kStages-deep ring, completing on the even CTA's "full" barriers, and the wgrad tail
+// steps; warp 1 lane 0 of the even CTA issues the pair's MMAs into one of two TMEM accumulators
+// (2 x 256 fp32 columns) and commits to the "empty" / "tmem full" barriers of both CTAs; warp 2
+// owns the TMEM allocation; warp 3 of each CTA zeroes wgrad tail rows; warps 4..11 of both
+// CTAs drain their TMEM rows (tcgen05.ld; two warps per 32-lane quarter, one per half of the
+// columns) and write the outputs while the next tile's MMAs run into the other accumulator.
 //
 // Determinism: each output element is produced by exactly one CTA pair, whose MMA sequence
 // is fixed by the unit's coordinates alone (never by the grid size or timing); the
