@@ -70,8 +70,11 @@ typedef enum gdg_status {
     GDG_EINVAL = 1,     /* null pointer, E outside [1, GDG_MAX_EXPERTS], N/K <= 0, rows < 0,
                            bad dtype or offs_kind, fwd/dgrad with fp32 out or accumulate,
                            bad split_rows */
-    GDG_EALIGN = 2,     /* N % 256 or K % 64 != 0 (the stable grouped GEMM API's shape rule
-                           on the docs page), or a pointer not 16-byte aligned */
+    GDG_EALIGN = 2,     /* N % 8 or K % 8 != 0 (every operand row must start on a 16-byte
+                           boundary for the TMA copies), or a pointer not 16-byte aligned.
+                           N and K need not be multiples of the 256-wide tiles: the docs
+                           page's stable-API rule (N % 256, K % 64) is relaxed, with rows and
+                           columns past N or K read as zeros and never written */
     GDG_EOVERLAP = 3,   /* out shares a byte with an input or the offsets (the accumulate
                            checks of the MoE grouped GEMM pull request) */
     GDG_EWORKSPACE = 4, /* workspace missing or smaller than grouped_det_gemm_workspace_bytes */

@@ -73,17 +73,8 @@ bool encode_prefetch(CUtensorMap* m, void* base, int64_t rows, int cols, bool fp
                       CU_TENSOR_MAP_SWIZZLE_NONE, base, 2, dims, strides, box);
 }
 
-// [rows, cols] bf16 seen as {64 columns, rows, cols/64 blocks}: one box {64, box_rows, 2}
-// brings two 64-column blocks of box_rows rows, each block box_rows x 128 B, one after the
-// other in shared memory.
-bool encode_row_blocks(CUtensorMap* m, const void* base, int64_t rows, int cols, uint32_t box_rows) {
-    const uint64_t dims[3] = {64, static_cast<uint64_t>(rows), static_cast<uint64_t>(cols / 64)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(cols) * 2, 128};
-    const uint32_t box[3] = {64, box_rows, 2};
-    return encode(m, base, 3, dims, strides, box);
-}
-
-// [rows, cols] bf16 as a plain 2-D map with box {64, box_rows} (wgrad tail steps).
+// [rows, cols] bf16 as a plain 2-D map with box {64, box_rows}: one copy brings one 64-column
+// block of box_rows rows (box_rows x 128 B); columns and rows past the extent read as zeros.
 bool encode_rows_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, uint32_t box_rows) {
     const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
     const uint64_t strides[1] = {static_cast<uint64_t>(cols) * 2};
@@ -91,15 +82,14 @@ bool encode_rows_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, ui
     return encode(m, base, 2, dims, strides, box);
 }
 
-// W [E, N, K] seen as {64 k, N, K/64 blocks, E}: box {64, 128, 2, 1} brings two 64-wide k
-// blocks of 128 n-rows of one expert (fwd: 128 n x 128 k; dgrad: 128 k x 128 n).
-bool encode_weight_blocks(CUtensorMap* m, const void* base, int E, int N, int K) {
-    const uint64_t dims[4] = {64, static_cast<uint64_t>(N), static_cast<uint64_t>(K / 64),
+// W [E, N, K] as {K, N, E} with box {64, 128, 1}: one copy brings 64 k-columns of 128 n-rows
+// of one expert (a box never crosses into another expert; past N or K it reads zeros).
+bool encode_weight_3d(CUtensorMap* m, const void* base, int E, int N, int K) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N),
                               static_cast<uint64_t>(E)};
-    const uint64_t strides[3] = {static_cast<uint64_t>(K) * 2, 128,
-                                 static_cast<uint64_t>(N) * K * 2};
-    const uint32_t box[4] = {64, 128, 2, 1};
-    return encode(m, base, 4, dims, strides, box);
+    const uint64_t strides[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    return encode(m, base, 3, dims, strides, box);
 }
 
 // ------------------------------------------------------------------ per-device caches
@@ -199,7 +189,7 @@ Range range_of(const void* p, uint64_t bytes) {
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int tiles_per_expert(int N, int K) {
-    return (N / gdg::kPairM) * static_cast<int>(ceil_div(K, gdg::kBN));
+    return static_cast<int>(ceil_div(N, gdg::kPairM) * ceil_div(K, gdg::kBN));
 }
 
 // Persistent grid: two CTAs per pair, at most one pair per unit.
@@ -233,7 +223,7 @@ gdg_status check_common(const gdg_args* args, const int32_t* offs, int E, int N,
         return GDG_EINVAL;
     if (args->offs_kind != GDG_OFFS_ENDS && args->offs_kind != GDG_OFFS_INDPTR) return GDG_EINVAL;
     if (out_dtype != GDG_BF16 && out_dtype != GDG_FP32) return GDG_EINVAL;
-    if (N % 256 != 0 || K % 64 != 0) return GDG_EALIGN;
+    if (N % 8 != 0 || K % 8 != 0) return GDG_EALIGN;   // 16-byte rows: TMA strides
     if (static_cast<int64_t>(E) * N * K > (int64_t{1} << 40)) return GDG_EINVAL;
     if (static_cast<int64_t>(E) * N >= INT32_MAX) return GDG_EINVAL;   // TMA row coordinates
     if (!offs) return GDG_EINVAL;
@@ -289,9 +279,9 @@ gdg_status plan_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N
 
     GemmParams& p = pl->p;
     std::memset(&p, 0, sizeof p);
-    if (!encode_weight_blocks(&p.tmA, args->b, E, N, K)) return GDG_ECUDA;
+    if (!encode_weight_3d(&p.tmA, args->b, E, N, K)) return GDG_ECUDA;
     for (int i = 0; i < 5; ++i)
-        if (!encode_row_blocks(&p.tmB[i], args->a, rows, in_cols, 8u << i)) return GDG_ECUDA;
+        if (!encode_rows_2d(&p.tmB[i], args->a, rows, in_cols, 8u << i)) return GDG_ECUDA;
     p.offs = offs;
     p.out = args->out;
     p.partial = nullptr;
@@ -306,7 +296,7 @@ gdg_status plan_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N
     // average only stream weights, and a 128-row tile keeps more weight bytes in flight
     // (larger groups lose more to re-reading weight tiles than they gain).
     pl->rt = (rows <= static_cast<int64_t>(E) * 64) ? 128 : 256;
-    const int64_t ft = (OP == gdg::OP_FWD) ? N / gdg::kPairM : ceil_div(K, gdg::kPairM);
+    const int64_t ft = (OP == gdg::OP_FWD) ? ceil_div(N, gdg::kPairM) : ceil_div(K, gdg::kPairM);
     const int64_t ub = ft * (ceil_div(rows, pl->rt) + E);
     if (ub > INT32_MAX) return GDG_EINVAL;
     p.max_units = static_cast<int>(ub);
@@ -366,8 +356,8 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
     const int64_t map_rows = rows > 0 ? rows : 1;
     const void* a = rows > 0 ? args->a : args->out;
     const void* b = rows > 0 ? args->b : args->out;
-    if (!encode_row_blocks(&p.tmA, a, map_rows, N, 128u) ||
-        !encode_row_blocks(&p.tmB[0], b, map_rows, K, 128u) ||
+    if (!encode_rows_2d(&p.tmA, a, map_rows, N, 128u) ||
+        !encode_rows_2d(&p.tmB[0], b, map_rows, K, 128u) ||
         !encode_rows_2d(&p.tmTail[0], a, map_rows, N, 16u) ||
         !encode_rows_2d(&p.tmTail[1], b, map_rows, K, 16u))
         return GDG_ECUDA;
@@ -488,13 +478,13 @@ gdg_status grouped_det_gemm_dgrad(const gdg_args* args, const int32_t* offs, int
 }
 
 int32_t grouped_det_gemm_auto_split_rows(int64_t rows, int E, int N, int K) {
-    if (E < 1 || N <= 0 || K <= 0 || N % 256 || K % 64 || rows < 0) return -1;
+    if (E < 1 || N <= 0 || K <= 0 || N % 8 || K % 8 || rows < 0) return -1;
     return auto_split_rows(rows, E, N, K);
 }
 
 size_t grouped_det_gemm_workspace_bytes(int op, int64_t rows, int E, int N, int K,
                                         gdg_dtype out_dtype, int accumulate, int32_t split_rows) {
-    if (E < 1 || E > GDG_MAX_EXPERTS || N <= 0 || K <= 0 || rows < 0 || N % 256 || K % 64 ||
+    if (E < 1 || E > GDG_MAX_EXPERTS || N <= 0 || K <= 0 || rows < 0 || N % 8 || K % 8 ||
         (out_dtype != GDG_BF16 && out_dtype != GDG_FP32) || op < GDG_OP_FWD || op > GDG_OP_WGRAD)
         return static_cast<size_t>(-1);
     (void)accumulate;
@@ -541,7 +531,7 @@ const char* gdg_status_string(gdg_status status) {
     switch (status) {
         case GDG_OK: return "ok";
         case GDG_EINVAL: return "invalid argument";
-        case GDG_EALIGN: return "shape or alignment rule violated (N % 256, K % 64, 16-byte pointers)";
+        case GDG_EALIGN: return "shape or alignment rule violated (N % 8, K % 8, 16-byte pointers)";
         case GDG_EOVERLAP: return "output overlaps an input, the offsets or the workspace";
         case GDG_EWORKSPACE: return "workspace missing or too small";
         case GDG_ECUDA: return "CUDA call failed";

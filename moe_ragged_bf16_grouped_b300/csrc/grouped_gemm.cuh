@@ -91,10 +91,12 @@ enum Epi : int { EPI_BF16 = 0, EPI_FP32 = 1, EPI_BF16_ACC = 2, EPI_FP32_ACC = 3,
 constexpr unsigned kDevErrTimeout = 6u;
 
 struct GemmParams {
-    CUtensorMap tmA;        // fwd / dgrad: W {k%64, n, k/64, e} box{64,128,2,1};
-                            // wgrad: G {n%64, row, n/64} box{64,128,2}
-    CUtensorMap tmB[5];     // fwd: X {k%64, row, k/64}, dgrad: G {n%64, row, n/64},
-                            // box{64, 8<<i, 2}; wgrad: tmB[0] = X {k%64, row, k/64} box{64,128,2}
+    // Operand maps (bf16, 128-byte swizzle, zero fill past every extent).  Every copy brings
+    // one 64-column block; a stage's two blocks land as consecutive sub-tiles.
+    CUtensorMap tmA;        // fwd / dgrad: W {K, N, E} box {64, 128, 1};
+                            // wgrad: G {N, rows} box {64, 128}
+    CUtensorMap tmB[5];     // fwd: X {K, rows}, dgrad: G {N, rows}, box {64, 8 << i};
+                            // wgrad: tmB[0] = X {K, rows} box {64, 128}
     CUtensorMap tmPre;      // wgrad accumulate: out as {K, E*N}, box {256, 128} (L2 prefetch)
     CUtensorMap tmTail[2];  // wgrad tail steps: G {N, rows}, X {K, rows}, box {64, 16}
     const int32_t* offs;
@@ -136,9 +138,9 @@ struct Shape {
 template <int OP>
 __device__ __forceinline__ Shape unit_shape(const GemmParams& p) {
     Shape s;
-    if (OP == OP_FWD) { s.ft = p.N / kPairM; s.kt = 1; }
+    if (OP == OP_FWD) { s.ft = (p.N + kPairM - 1) / kPairM; s.kt = 1; }
     else if (OP == OP_DGRAD) { s.ft = (p.K + kPairM - 1) / kPairM; s.kt = 1; }
-    else { s.kt = (p.K + kBN - 1) / kBN; s.ft = (p.N / kPairM) * s.kt; }
+    else { s.kt = (p.K + kBN - 1) / kBN; s.ft = ((p.N + kPairM - 1) / kPairM) * s.kt; }
     return s;
 }
 
@@ -503,9 +505,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                            ? 2u * (kABytes + R::kBBytes)
                                            : 2u * (kABytes + (8u << bi) * 256u);
                 const int fa = t.f0 + kBM * static_cast<int>(pr.rank);   // this CTA's A rows
-                if (OP == OP_WGRAD && (EPI == EPI_FP32_ACC || EPI == EPI_BF16_ACC))
+                if (OP == OP_WGRAD && (EPI == EPI_FP32_ACC || EPI == EPI_BF16_ACC) &&
+                    fa + kBM <= p.N)
                     // The epilogue reads this CTA's 128 x 256 block of out after the unit's
-                    // mainloop: start bringing it into L2 now.
+                    // mainloop: start bringing it into L2 now (whole 128-row blocks only, so
+                    // the box never reaches past the last expert's rows).
                     tma_prefetch_2d(&p.tmPre, t.c0, t.e * p.N + fa);
                 if (OP == OP_WGRAD) {
                     const int v = tail_rows(t.nred, t.nkb);
@@ -534,25 +538,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     uint8_t* b = a + kABytes;
                     const uint32_t fb = full0 + stage * 8u;
                     if (even) mbar_arrive_expect_tx(&c->full[stage], bytes);
-                    // One copy per operand and stage: each map's third dimension walks
-                    // 64-column blocks, so two blocks land as consecutive sub-tiles (a block
-                    // past the tensor's extent reads as zeros).
-                    if (OP == OP_FWD) {
-                        // A: 128 n-rows of W[e] x k blocks 2kb, 2kb+1; B: rows x the same k.
-                        tma_load_4d_pair(a, &p.tmA, fb, 0, fa, 2 * kb, t.e);
-                        tma_load_3d_pair(b, &p.tmB[bi], fb, 0,
-                                         t.c0 + half * static_cast<int>(pr.rank), 2 * kb);
-                    } else if (OP == OP_DGRAD) {
-                        // A: n-rows 128kb.. of W[e] x this CTA's two 64-wide k blocks.
-                        tma_load_4d_pair(a, &p.tmA, fb, 0, kb * kBK, fa / 64, t.e);
-                        tma_load_3d_pair(b, &p.tmB[bi], fb, 0,
-                                         t.c0 + half * static_cast<int>(pr.rank), 2 * kb);
+                    // Two copies per operand and stage, one per 64-column block, landing as
+                    // consecutive sub-tiles.  Columns and rows past a tensor's extent read as
+                    // zeros, so N and K need not be multiples of the tile (every x coordinate
+                    // is a multiple of 64 elements).
+                    const int kx = kb * kBK;
+                    if (OP == OP_FWD || OP == OP_DGRAD) {
+                        // fwd A: 128 n-rows of W[e] from fa x k columns kx, kx + 64.
+                        // dgrad A: n-rows kx.. of W[e] x this CTA's k columns fa, fa + 64.
+                        const int ax = OP == OP_FWD ? kx : fa, ay = OP == OP_FWD ? fa : kx;
+                        tma_load_3d_pair(a, &p.tmA, fb, ax, ay, t.e);
+                        tma_load_3d_pair(a + kSubBytes, &p.tmA, fb, ax + 64, ay, t.e);
+                        // B: packed rows of this CTA's half x the stage's reduction columns.
+                        const int rb = t.c0 + half * static_cast<int>(pr.rank);
+                        tma_load_2d_pair(b, &p.tmB[bi], fb, kx, rb);
+                        tma_load_2d_pair(b + (8 << bi) * 128, &p.tmB[bi], fb, kx + 64, rb);
                     } else {
                         // 128 reduction rows x this CTA's two 64-wide blocks of G and of X.
                         const int r = t.r0 + kb * kBK;
-                        tma_load_3d_pair(a, &p.tmA, fb, 0, r, fa / 64);
-                        tma_load_3d_pair(b, &p.tmB[0], fb, 0, r,
-                                         (t.c0 + (kBN / 2) * static_cast<int>(pr.rank)) / 64);
+                        const int xb = t.c0 + (kBN / 2) * static_cast<int>(pr.rank);
+                        tma_load_2d_pair(a, &p.tmA, fb, fa, r);
+                        tma_load_2d_pair(a + kSubBytes, &p.tmA, fb, fa + 64, r);
+                        tma_load_2d_pair(b, &p.tmB[0], fb, xb, r);
+                        tma_load_2d_pair(b + kSubBytes, &p.tmB[0], fb, xb + 64, r);
                     }
                     if (++stage == R::kStages) { stage = 0; phase ^= 1u; }
                 }
@@ -722,15 +730,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         (static_cast<size_t>(t.e) * p.N + t.f0 + mrow0) * ldo +
                         static_cast<size_t>(t.c0) * osz;
             }
-            // This warp's 64 or 128 columns as boxes of 32 rows x 64 bytes (16 fp32 or 32
-            // bf16 columns; K % 64 == 0, so a warp has 0, 2 or 4 bf16 / 0, 4 or 8 fp32 boxes).
-            // Box b is bytes [64 b, 64 b + 64) of the warp's row segments.  With accumulate,
-            // the old values of the next kAhead boxes are always in flight.
+            // This warp's (up to) 128 columns as boxes of 32 rows x 64 bytes (16 fp32 or 32
+            // bf16 columns; up to 8 or 4 boxes).  Box b is bytes [64 b, 64 b + 64) of the
+            // warp's row segments.  With accumulate, the old values of the next kAhead boxes
+            // are always in flight.  A row past N or a 16-byte chunk past K (K % 8 == 0, so a
+            // chunk is all in or all out) is neither read nor written; the split form's partial
+            // tiles are written whole.
             constexpr int kBoxCols = f32 ? 16 : 32;
             constexpr int kPer = 32 / kBoxCols;             // boxes per 32 TMEM columns
             constexpr int kBoxes = 128 / kBoxCols;
             constexpr int kAhead = acc ? 3 : 1;
-            const int nbox = max(0, cend - 128 * hc) / kBoxCols;
+            constexpr int kChunkCols = 16 / osz;
+            const int nbox = (max(0, cend - 128 * hc) + kBoxCols - 1) / kBoxCols;
+            const int nvalid = EPI == EPI_PARTIAL ? 32 : p.N - (t.f0 + mrow0);   // rows of the warp
+            const int kvalid = EPI == EPI_PARTIAL ? 128 : p.K - (t.c0 + 128 * hc);
+            auto inside = [&](int b, int j) {
+                return rr + 8 * j < nvalid && b * kBoxCols + gg * kChunkCols < kvalid;
+            };
             uint8_t* gseg = obase + static_cast<size_t>(rr) * ldo + (128 * hc) * osz + gg * 16;
             uint4 old[kAhead][4];
             auto first_loads = [&]() {
@@ -740,7 +756,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (b < nbox)
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
-                                old[b][j] = *reinterpret_cast<const uint4*>(gseg + b * 64 + 8 * j * ldo);
+                                old[b][j] = inside(b, j) ? *reinterpret_cast<const uint4*>(
+                                                              gseg + b * 64 + 8 * j * ldo)
+                                                        : make_uint4(0, 0, 0, 0);
                 }
             };
             int fb = A;                 // the buffer that ends up holding the unit's value
@@ -846,14 +864,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             v.w = pack_bf16x2(__fadd_rn(bf16_lo(o.w), bf16_lo(v.w)), __fadd_rn(bf16_hi(o.w), bf16_hi(v.w)));
                         }
                     }
-                    *reinterpret_cast<uint4*>(gline + 8 * j * ldo) = v;
+                    if (inside(b, j)) *reinterpret_cast<uint4*>(gline + 8 * j * ldo) = v;
                 }
                 if constexpr (acc) {
                     if (b + kAhead < nbox)
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            old[b % kAhead][j] =
-                                *reinterpret_cast<const uint4*>(gseg + (b + kAhead) * 64 + 8 * j * ldo);
+                            old[b % kAhead][j] = inside(b + kAhead, j)
+                                                     ? *reinterpret_cast<const uint4*>(
+                                                           gseg + (b + kAhead) * 64 + 8 * j * ldo)
+                                                     : make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();   // the box is rewritten by the next box
             }
@@ -953,7 +973,7 @@ __global__ void __launch_bounds__(kReduceThreads) wgrad_reduce_kernel(const __gr
     __shared__ ReduceSmem sm;
     Shape sh;
     sh.kt = (p.K + kBN - 1) / kBN;
-    sh.ft = (p.N / kPairM) * sh.kt;
+    sh.ft = ((p.N + kPairM - 1) / kPairM) * sh.kt;
     build_schedule<OP_WGRAD>(p.offs, p.offs_kind, p.rows, p.E, p.split_rows, p.max_units, sh,
                              sm.start, sm.size, sm.prefix, sm.warp_tot, &sm.total);
     const int64_t NK = static_cast<int64_t>(p.N) * p.K;

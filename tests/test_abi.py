@@ -67,8 +67,8 @@ def test_refusals_before_launch(lib, op):
     assert call(lib, op, good(), OFFS, 1025, 256, 256) == EINVAL
     assert call(lib, op, good(rows=-1), OFFS, 4, 256, 256) == EINVAL
     assert call(lib, op, good(kind=2), OFFS, 4, 256, 256) == EINVAL
-    assert call(lib, op, good(), OFFS, 4, 128, 256) == EALIGN      # N % 256
-    assert call(lib, op, good(), OFFS, 4, 256, 96) == EALIGN       # K % 64
+    assert call(lib, op, good(), OFFS, 4, 132, 256) == EALIGN      # N % 8: rows not 16-byte aligned
+    assert call(lib, op, good(), OFFS, 4, 256, 100) == EALIGN      # K % 8
     assert call(lib, op, good(), OFFS, 4, 256, 256, dtype=7) == EINVAL
     bad = good()
     bad.out = OUT + 8
@@ -114,6 +114,9 @@ def test_workspace_bytes_and_auto_form(lib):
     assert f(2, 512, 4, 256, 256, 1, 1, 64) == 12 * 256 * 256 * 4
     assert f(2, 512, 4, 256, 256, 0, 0, 100) == ctypes.c_size_t(-1).value
     assert f(3, 512, 4, 256, 256, 0, 0, 0) == ctypes.c_size_t(-1).value
+    # N, K that are not tile multiples round the tiles up: N=264, K=328 -> 2 x 2 tiles per expert
+    assert f(2, 512, 4, 264, 328, 1, 1, 64) == 4 * 12 * 256 * 256 * 4
+    assert f(2, 512, 4, 260, 328, 1, 1, 64) == ctypes.c_size_t(-1).value   # N % 8
     # the automatic form depends on shapes only
     assert g(16384, 8, 14336, 4096) == -1          # many tiles: unsplit
     assert g(65536, 64, 1536, 2048) == -1
@@ -146,7 +149,7 @@ def test_plan_refusals_leave_no_plan(lib):
         assert lib.gdg_plan_create(op, ctypes.byref(good()), OFFS, E, 256, 256, dtype, acc,
                                    ctypes.byref(h)) == EINVAL
         assert h.value is None
-    assert lib.gdg_plan_create(0, ctypes.byref(good()), OFFS, 4, 128, 256, 0, 0,
+    assert lib.gdg_plan_create(0, ctypes.byref(good()), OFFS, 4, 132, 256, 0, 0,
                                ctypes.byref(h)) == EALIGN
     assert lib.gdg_plan_create(2, ctypes.byref(good(split=64)), OFFS, 4, 256, 256, 0, 0,
                                ctypes.byref(h)) == EWORKSPACE
