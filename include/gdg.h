@@ -107,6 +107,15 @@ typedef enum gdg_op { GDG_OP_FWD = 0, GDG_OP_DGRAD = 1, GDG_OP_WGRAD = 2 } gdg_o
  *       p0 + p1 + ... before rounding or accumulating.
  * workspace / workspace_bytes: device scratch for the split form, at least
  * grouped_det_gemm_workspace_bytes(...) bytes; ignored when that is 0.
+ *
+ * Output strides (the accumulate contract of the MoE grouped GEMM pull request allows a
+ * main_grad that is a strided view with unit stride along K): out element (row, col) of
+ * fwd / dgrad is at out[row * out_ld + col], element (e, n, k) of wgrad at
+ * out[e * out_es + n * out_ld + k]; 0 means the dense value (N or K for out_ld,
+ * N * out_ld for out_es).  Each stride times the element size must be a multiple of 16
+ * bytes (GDG_EALIGN), and no two output elements may share memory (GDG_EOVERLAP: rows of
+ * out_ld < columns, or experts whose row ranges interleave or overlap).  Inputs (a, b) are
+ * always dense.
  */
 typedef struct gdg_args {
     const void* a;
@@ -117,6 +126,8 @@ typedef struct gdg_args {
     int64_t rows;
     int32_t offs_kind;
     int32_t split_rows;
+    int64_t out_ld;     /* row stride of out, in elements (0: dense) */
+    int64_t out_es;     /* wgrad: expert stride of out, in elements (0: dense); 0 for fwd/dgrad */
 } gdg_args;
 
 /* Forward projection (docs page table, row "fwd"). out_dtype must be GDG_BF16 and

@@ -47,7 +47,8 @@ class GdgArgs(ctypes.Structure):
     _fields_ = [("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("out", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("rows", ctypes.c_int64), ("offs_kind", ctypes.c_int32),
-                ("split_rows", ctypes.c_int32)]
+                ("split_rows", ctypes.c_int32), ("out_ld", ctypes.c_int64),
+                ("out_es", ctypes.c_int64)]
 
 
 for _name in ("grouped_det_gemm_fwd", "grouped_det_gemm_dgrad", "grouped_det_gemm_wgrad",
@@ -131,6 +132,29 @@ def _check_operand(t: torch.Tensor, name: str, dtype=torch.bfloat16, ndim=None):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _check_out(t: torch.Tensor, dtype, ndim: int):
+    """An output may be a strided view (unit stride along its last dimension); the library
+    checks alignment and that no two elements share memory."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("out must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"out must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"out must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError("out must be on a CUDA device")
+    if t.numel() and t.stride(-1) != 1:
+        raise ValueError("out must have unit stride along its last dimension")
+
+
+def _out_strides(out: torch.Tensor):
+    """(row stride, expert stride) in elements for the C ABI; 0 (dense) where a dimension has
+    a single entry, whose stride torch does not pin down."""
+    ld = out.stride(-2) if out.shape[-2] > 1 else 0
+    es = (out.stride(0) if out.shape[0] > 1 else 0) if out.dim() == 3 else 0
+    return ld, es
+
+
 def _offs_kind(offs_kind) -> int:
     if offs_kind in (GDG_OFFS_ENDS, "ends", "offs"):
         return GDG_OFFS_ENDS
@@ -165,10 +189,11 @@ def _fwd_args(x, w, offs, out, offs_kind):
         raise ValueError("shape mismatch between x, w and offs")
     if out is None:
         out = torch.empty((x.shape[0], N), dtype=torch.bfloat16, device=x.device)
-    _check_operand(out, "out", ndim=2)
+    _check_out(out, torch.bfloat16, 2)
     if tuple(out.shape) != (x.shape[0], N):
         raise ValueError("out must be [rows, N]")
-    args = GdgArgs(x.data_ptr(), w.data_ptr(), out.data_ptr(), None, 0, x.shape[0], kind, 0)
+    args = GdgArgs(x.data_ptr(), w.data_ptr(), out.data_ptr(), None, 0, x.shape[0], kind, 0,
+                   *_out_strides(out))
     return args, (E, N, K, GDG_BF16, 0), out, (x, w, offs, out)
 
 
@@ -181,10 +206,11 @@ def _dgrad_args(g, w, offs, out, offs_kind):
         raise ValueError("shape mismatch between g, w and offs")
     if out is None:
         out = torch.empty((g.shape[0], K), dtype=torch.bfloat16, device=g.device)
-    _check_operand(out, "out", ndim=2)
+    _check_out(out, torch.bfloat16, 2)
     if tuple(out.shape) != (g.shape[0], K):
         raise ValueError("out must be [rows, K]")
-    args = GdgArgs(g.data_ptr(), w.data_ptr(), out.data_ptr(), None, 0, g.shape[0], kind, 0)
+    args = GdgArgs(g.data_ptr(), w.data_ptr(), out.data_ptr(), None, 0, g.shape[0], kind, 0,
+                   *_out_strides(out))
     return args, (E, N, K, GDG_BF16, 0), out, (g, w, offs, out)
 
 
@@ -206,7 +232,7 @@ def _wgrad_args(g, x, offs, out, out_dtype, num_groups, accumulate, split_rows, 
         out = torch.empty((E, N, K), dtype=out_dtype or torch.bfloat16, device=g.device)
     if out_dtype is not None and out_dtype != out.dtype:
         raise ValueError("out_dtype must be None or out.dtype")
-    _check_operand(out, "out", out.dtype, 3)
+    _check_out(out, out.dtype, 3)
     if tuple(out.shape) != (E, N, K):
         raise ValueError("out must be [E, N, K]")
     code = _dtype_code(out.dtype)
@@ -217,7 +243,7 @@ def _wgrad_args(g, x, offs, out, out_dtype, num_groups, accumulate, split_rows, 
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     args = GdgArgs(g.data_ptr(), x.data_ptr(), out.data_ptr(), ws_ptr, ws_bytes, rows, kind,
-                   split_rows)
+                   split_rows, *_out_strides(out))
     return args, (E, N, K, code, int(accumulate)), out, (g, x, offs, out, workspace)
 
 
@@ -328,10 +354,11 @@ def grouped_det_gemm_wgrad_noalloc(g: torch.Tensor, x: torch.Tensor, offs: torch
         raise ValueError("g and x must have the same number of rows")
     K = x.shape[1]
     E = _num_groups(offs, kind)
-    _check_operand(out, "out", out.dtype, 3)
+    _check_out(out, out.dtype, 3)
     if tuple(out.shape) != (E, N, K):
         raise ValueError("out must be [E, N, K]")
-    args = GdgArgs(g.data_ptr(), x.data_ptr(), out.data_ptr(), None, 0, rows, kind, split_rows)
+    args = GdgArgs(g.data_ptr(), x.data_ptr(), out.data_ptr(), None, 0, rows, kind, split_rows,
+                   *_out_strides(out))
     _call(_lib.grouped_det_gemm_wgrad_noalloc, "grouped_det_gemm_wgrad_noalloc", args, offs, E,
           N, K, _dtype_code(out.dtype), int(accumulate), _stream_ptr(stream, g.device))
     return out

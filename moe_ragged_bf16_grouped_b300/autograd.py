@@ -9,8 +9,8 @@ library's kernels; this module only routes tensors.
 convention that the MoE grouped GEMM pull request adopts for the deterministic wrapper
 (section "Deterministic weight-gradient accumulation"):
 
-- ``w.main_grad`` (fp32 or bf16, w's shape and device; here also contiguous) is checked when the
-  forward runs and read again by the backward;
+- ``w.main_grad`` (fp32 or bf16, w's shape and device, unit stride along its last dimension; a
+  strided view is fine) is checked when the forward runs and read again by the backward;
 - the backward adds the deterministic dW into it with the fused accumulate (the bits of
   ``main_grad.add_(dW)``), every time it runs: ``retain_graph`` and a second backward add twice,
   and so does ``torch.autograd.grad`` whose inputs exclude w;
@@ -40,8 +40,8 @@ def _check_main_grad(w: torch.Tensor) -> torch.Tensor:
         raise TypeError(f"w.main_grad must be float32 or bfloat16, got {mg.dtype}")
     if tuple(mg.shape) != tuple(w.shape) or mg.device != w.device:
         raise ValueError("w.main_grad must have w's shape and device")
-    if not mg.is_contiguous():
-        raise ValueError("w.main_grad must be contiguous")
+    if mg.stride(-1) != 1:
+        raise ValueError("w.main_grad must have unit stride along its last dimension")
     return mg
 
 

@@ -10,6 +10,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <utility>
 
 #include "gdg.h"
 #include "grouped_gemm.cuh"
@@ -64,13 +65,17 @@ bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                       dims, strides_bytes, box);
 }
 
-// wgrad accumulate: out [rows, cols] (bf16 or fp32) for L2 prefetches of 128 x 256 blocks.
-bool encode_prefetch(CUtensorMap* m, void* base, int64_t rows, int cols, bool fp32) {
-    const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(cols) * (fp32 ? 4u : 2u)};
-    const uint32_t box[2] = {256u, 128u};
+// wgrad accumulate: out [E, N, K] (bf16 or fp32, row stride ld, expert stride es, in
+// elements) for L2 prefetches of 128 x 256 blocks of one expert.
+bool encode_prefetch(CUtensorMap* m, void* base, int E, int N, int K, int64_t ld, int64_t es,
+                     bool fp32) {
+    const uint64_t esz = fp32 ? 4u : 2u;
+    const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                              static_cast<uint64_t>(E)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(ld) * esz, static_cast<uint64_t>(es) * esz};
+    const uint32_t box[3] = {256u, 128u, 1u};
     return encode_map(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      CU_TENSOR_MAP_SWIZZLE_NONE, base, 2, dims, strides, box);
+                      CU_TENSOR_MAP_SWIZZLE_NONE, base, 3, dims, strides, box);
 }
 
 // [rows, cols] bf16 as a plain 2-D map with box {64, box_rows}: one copy brings one 64-column
@@ -188,6 +193,38 @@ Range range_of(const void* p, uint64_t bytes) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// The output's strides (elements) and the bytes it spans, from out_ld / out_es (0 = dense).
+struct OutLayout {
+    int64_t ld = 0, es = 0;
+    uint64_t span = 0;
+};
+
+// out is [E][n][cols] with unit stride along cols (E = 1 and no expert stride for fwd / dgrad).
+// Strides must keep every row on a 16-byte boundary (the epilogues store 16-byte chunks), and
+// no two elements may share memory: taken in increasing order of stride, the row and expert
+// strides must each reach past everything below them.
+gdg_status out_layout(const gdg_args* a, int64_t n, int64_t cols, int64_t E, uint64_t esz,
+                      bool wgrad, OutLayout* L) {
+    if (a->out_ld < 0 || a->out_es < 0 || (!wgrad && a->out_es != 0)) return GDG_EINVAL;
+    const int64_t ld = a->out_ld ? a->out_ld : cols;
+    const int64_t es = !wgrad ? 0 : (a->out_es ? a->out_es : n * ld);
+    if ((static_cast<uint64_t>(ld) * esz) % 16 != 0 || (static_cast<uint64_t>(es) * esz) % 16 != 0)
+        return GDG_EALIGN;
+    int64_t s1 = ld, n1 = n, s2 = es, n2 = E;       // (stride, extent) of the two outer dims
+    if (n1 <= 1) { s1 = s2; n1 = n2; s2 = 0; n2 = 1; }
+    if (n2 > 1 && s2 < s1) { std::swap(s1, s2); std::swap(n1, n2); }
+    const int64_t below1 = cols;                     // span of the dims under the first
+    if (n1 > 1 && s1 < below1) return GDG_EOVERLAP;
+    const int64_t below2 = (n1 > 1 ? (n1 - 1) * s1 : 0) + cols;
+    if (n2 > 1 && s2 < below2) return GDG_EOVERLAP;
+    if (static_cast<double>(E - 1) * es + static_cast<double>(n - 1) * ld + cols > 9.0e15)
+        return GDG_EINVAL;
+    L->ld = ld;
+    L->es = es;
+    L->span = static_cast<uint64_t>((E - 1) * es + (n > 0 ? (n - 1) * ld : 0) + cols) * esz;
+    return GDG_OK;
+}
+
 int tiles_per_expert(int N, int K) {
     return static_cast<int>(ceil_div(N, gdg::kPairM) * ceil_div(K, gdg::kBN));
 }
@@ -268,7 +305,10 @@ gdg_status plan_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N
         return GDG_EALIGN;
     const int in_cols = (OP == gdg::OP_FWD) ? K : N;     // columns of the row operand
     const int out_cols = (OP == gdg::OP_FWD) ? N : K;
-    const Range r_out = range_of(args->out, static_cast<uint64_t>(rows) * out_cols * 2);
+    OutLayout L;
+    st = out_layout(args, rows, out_cols, 1, 2, false, &L);
+    if (st != GDG_OK) return st;
+    const Range r_out = range_of(args->out, L.span);
     const Range r_a = range_of(args->a, static_cast<uint64_t>(rows) * in_cols * 2);
     const Range r_b = range_of(args->b, static_cast<uint64_t>(E) * N * K * 2);
     const Range r_o = range_of(offs, static_cast<uint64_t>(E + args->offs_kind) * 4);
@@ -292,6 +332,7 @@ gdg_status plan_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N
     p.K = K;
     p.offs_kind = args->offs_kind;
     p.split_rows = 0;
+    p.ld_out = L.ld;
     // Row tile (and ring geometry), from the shapes alone: groups of at most 64 rows on
     // average only stream weights, and a 128-row tile keeps more weight bytes in flight
     // (larger groups lose more to re-reading weight tiles than they gain).
@@ -319,7 +360,10 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
                                                                    !aligned16(args->b))))
         return GDG_EALIGN;
     const size_t osz = out_dtype == GDG_FP32 ? 4 : 2;
-    const Range r_out = range_of(args->out, static_cast<uint64_t>(E) * N * K * osz);
+    OutLayout L;
+    st = out_layout(args, N, K, E, osz, true, &L);
+    if (st != GDG_OK) return st;
+    const Range r_out = range_of(args->out, L.span);
     const Range r_a = range_of(args->a, static_cast<uint64_t>(rows) * N * 2);
     const Range r_b = range_of(args->b, static_cast<uint64_t>(rows) * K * 2);
     const Range r_o = range_of(offs, static_cast<uint64_t>(E + args->offs_kind) * 4);
@@ -361,9 +405,10 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
         !encode_rows_2d(&p.tmTail[0], a, map_rows, N, 16u) ||
         !encode_rows_2d(&p.tmTail[1], b, map_rows, K, 16u))
         return GDG_ECUDA;
-    if (!split && accumulate &&
-        !encode_prefetch(&p.tmPre, args->out, static_cast<int64_t>(E) * N, K,
-                         out_dtype == GDG_FP32))
+    // The prefetch map takes the common layouts (experts in address order, rows in order).
+    p.prefetch = !split && accumulate && L.es >= static_cast<int64_t>(N) * L.ld;
+    if (p.prefetch &&
+        !encode_prefetch(&p.tmPre, args->out, E, N, K, L.ld, L.es, out_dtype == GDG_FP32))
         return GDG_ECUDA;
     p.offs = offs;
     p.out = args->out;
@@ -376,6 +421,8 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
     p.offs_kind = args->offs_kind;
     p.split_rows = split ? split_rows : 0;
     p.max_units = static_cast<int>(max_units);
+    p.ld_out = L.ld;
+    p.es_out = L.es;
     pl->grid = pair_grid(max_units, dev->pairs);
     pl->epi = split ? static_cast<int>(gdg::EPI_PARTIAL) : epi;
     pl->launch = true;
@@ -393,6 +440,8 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
         r.epi = epi;
         r.split_rows = split_rows;
         r.max_units = static_cast<int>(max_units);
+        r.ld_out = L.ld;
+        r.es_out = L.es;
         const int64_t vec4 = static_cast<int64_t>(E) * N * K / 4;
         int64_t rgrid = ceil_div(vec4, gdg::kReduceThreads);
         if (rgrid > static_cast<int64_t>(dev->sms) * 8) rgrid = static_cast<int64_t>(dev->sms) * 8;

@@ -97,7 +97,8 @@ struct GemmParams {
                             // wgrad: G {N, rows} box {64, 128}
     CUtensorMap tmB[5];     // fwd: X {K, rows}, dgrad: G {N, rows}, box {64, 8 << i};
                             // wgrad: tmB[0] = X {K, rows} box {64, 128}
-    CUtensorMap tmPre;      // wgrad accumulate: out as {K, E*N}, box {256, 128} (L2 prefetch)
+    CUtensorMap tmPre;      // wgrad accumulate: out as {K, N, E} (its strides), box {256, 128, 1}
+                            // (L2 prefetch; only when prefetch != 0)
     CUtensorMap tmTail[2];  // wgrad tail steps: G {N, rows}, X {K, rows}, box {64, 16}
     const int32_t* offs;
     void* out;
@@ -108,6 +109,9 @@ struct GemmParams {
     int offs_kind;
     int split_rows;         // wgrad: > 0 selects the split form
     int max_units;          // units at or past this index are skipped
+    int prefetch;           // wgrad accumulate: tmPre is valid
+    int64_t ld_out;         // out row stride (elements)
+    int64_t es_out;         // wgrad: out expert stride (elements)
 };
 
 struct SmemCtl {
@@ -506,11 +510,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                            : 2u * (kABytes + (8u << bi) * 256u);
                 const int fa = t.f0 + kBM * static_cast<int>(pr.rank);   // this CTA's A rows
                 if (OP == OP_WGRAD && (EPI == EPI_FP32_ACC || EPI == EPI_BF16_ACC) &&
-                    fa + kBM <= p.N)
+                    p.prefetch && fa + kBM <= p.N)
                     // The epilogue reads this CTA's 128 x 256 block of out after the unit's
-                    // mainloop: start bringing it into L2 now (whole 128-row blocks only, so
-                    // the box never reaches past the last expert's rows).
-                    tma_prefetch_2d(&p.tmPre, t.c0, t.e * p.N + fa);
+                    // mainloop: start bringing it into L2 now (whole 128-row blocks only).
+                    tma_prefetch_3d(&p.tmPre, t.c0, fa, t.e);
                 if (OP == OP_WGRAD) {
                     const int v = tail_rows(t.nred, t.nkb);
                     if (v) {
@@ -725,10 +728,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         (static_cast<size_t>(t.u) * kPairM + mrow0) * kBN * 4;
                 ldo = static_cast<size_t>(kBN) * 4;
             } else {
-                ldo = static_cast<size_t>(p.K) * osz;
+                ldo = static_cast<size_t>(p.ld_out) * osz;
                 obase = reinterpret_cast<uint8_t*>(p.out) +
-                        (static_cast<size_t>(t.e) * p.N + t.f0 + mrow0) * ldo +
-                        static_cast<size_t>(t.c0) * osz;
+                        (static_cast<size_t>(t.e) * p.es_out +
+                         static_cast<size_t>(t.f0 + mrow0) * p.ld_out + t.c0) * osz;
             }
             // This warp's (up to) 128 columns as boxes of 32 rows x 64 bytes (16 fp32 or 32
             // bf16 columns; up to 8 or 4 boxes).  Box b is bytes [64 b, 64 b + 64) of the
@@ -921,7 +924,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (j < jn)
-                            out[(row + j) * fdim + f] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                            out[(row + j) * p.ld_out + f] = __float2bfloat16_rn(__uint_as_float(r[j]));
                 }
             }
             tc_fence_before();
@@ -957,6 +960,7 @@ struct ReduceParams {
     int epi;            // EPI_BF16 / EPI_FP32 / EPI_BF16_ACC / EPI_FP32_ACC
     int split_rows;
     int max_units;
+    int64_t ld_out, es_out;   // out strides (elements)
 };
 
 struct ReduceSmem {
@@ -998,15 +1002,17 @@ __global__ void __launch_bounds__(kReduceThreads) wgrad_reduce_kernel(const __gr
             else acc = make_float4(__fadd_rn(acc.x, v.x), __fadd_rn(acc.y, v.y),
                                    __fadd_rn(acc.z, v.z), __fadd_rn(acc.w, v.w));
         }
+        // Four consecutive k of one row (K % 8 == 0): one 16-byte (fp32) or 8-byte (bf16) access.
+        const int64_t off = static_cast<int64_t>(e) * p.es_out + static_cast<int64_t>(n) * p.ld_out + k;
         if (p.epi == EPI_FP32) {
-            reinterpret_cast<float4*>(p.out)[i] = acc;
+            *reinterpret_cast<float4*>(static_cast<float*>(p.out) + off) = acc;
         } else if (p.epi == EPI_FP32_ACC) {
-            float4* o = reinterpret_cast<float4*>(p.out) + i;
+            float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off);
             const float4 old = *o;
             *o = make_float4(__fadd_rn(old.x, acc.x), __fadd_rn(old.y, acc.y),
                              __fadd_rn(old.z, acc.z), __fadd_rn(old.w, acc.w));
         } else {
-            uint2* o = reinterpret_cast<uint2*>(p.out) + i;
+            uint2* o = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + off);
             uint2 d;
             d.x = pack_bf16x2(acc.x, acc.y);
             d.y = pack_bf16x2(acc.z, acc.w);

@@ -221,9 +221,10 @@ __device__ __forceinline__ void bulk_wait_group() {
 }
 
 // Brings a tile of the tensor into L2 (no shared memory involved).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(m),
-                 "r"(x), "r"(y)
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int32_t x, int32_t y,
+                                                int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(m),
+                 "r"(x), "r"(y), "r"(z)
                  : "memory");
 }
 

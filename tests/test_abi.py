@@ -38,7 +38,8 @@ class Args(ctypes.Structure):
     _fields_ = [("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("out", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("rows", ctypes.c_int64), ("offs_kind", ctypes.c_int32),
-                ("split_rows", ctypes.c_int32)]
+                ("split_rows", ctypes.c_int32),
+                ("out_ld", ctypes.c_int64), ("out_es", ctypes.c_int64)]
 
 
 def call(lib, op, args, offs, E, N, K, dtype=0, acc=0):
@@ -97,6 +98,36 @@ def test_wgrad_refusals(lib):
     ws = good(split=64)
     ws.workspace, ws.workspace_bytes = A + 4096, 1 << 30                    # scratch over an input
     assert call(lib, op, ws, OFFS, 4, 256, 256) == EOVERLAP
+
+
+def strided(ld=0, es=0, rows=512):
+    a = good(rows=rows)
+    a.out_ld, a.out_es = ld, es
+    return a
+
+
+@pytest.mark.parametrize("op", ["grouped_det_gemm_fwd", "grouped_det_gemm_dgrad"])
+def test_output_stride_refusals_fwd_dgrad(lib, op):
+    """Row strides of Y / dX: 16-byte multiples that reach past a row; no expert stride."""
+    assert call(lib, op, strided(ld=-8), OFFS, 4, 256, 256) == EINVAL
+    assert call(lib, op, strided(es=8), OFFS, 4, 256, 256) == EINVAL         # fwd/dgrad: 2-D out
+    assert call(lib, op, strided(ld=260), OFFS, 4, 256, 256) == EALIGN       # 520 B rows
+    assert call(lib, op, strided(ld=248), OFFS, 4, 256, 256) == EOVERLAP     # rows overlap
+
+
+def test_output_stride_refusals_wgrad(lib):
+    """dW / main_grad strides: aligned, and no two of the E x N x K elements at one address."""
+    op = "grouped_det_gemm_wgrad"
+    assert call(lib, op, strided(ld=-8), OFFS, 4, 256, 256) == EINVAL
+    assert call(lib, op, strided(ld=260), OFFS, 4, 256, 256) == EALIGN       # bf16: 520 B
+    assert call(lib, op, strided(ld=258), OFFS, 4, 256, 256, dtype=1) == EALIGN   # fp32: 1032 B
+    assert call(lib, op, strided(ld=128), OFFS, 4, 256, 256) == EOVERLAP     # rows overlap
+    # experts 8 elements short of N rows: the last row of expert e meets expert e + 1
+    assert call(lib, op, strided(ld=256, es=256 * 256 - 8), OFFS, 4, 256, 256) == EOVERLAP
+    # experts interleaved row by row but rows only 2 experts apart: rows collide
+    assert call(lib, op, strided(ld=512, es=256), OFFS, 4, 256, 256) == EOVERLAP
+    # the same refusals hold for accumulate (main_grad views) and through the plan API
+    assert call(lib, op, strided(ld=128), OFFS, 4, 256, 256, dtype=1, acc=1) == EOVERLAP
 
 
 def test_workspace_bytes_and_auto_form(lib):

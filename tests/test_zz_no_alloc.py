@@ -26,7 +26,8 @@ class Args(ctypes.Structure):
     _fields_ = [("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("out", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("rows", ctypes.c_int64), ("offs_kind", ctypes.c_int32),
-                ("split_rows", ctypes.c_int32)]
+                ("split_rows", ctypes.c_int32),
+                ("out_ld", ctypes.c_int64), ("out_es", ctypes.c_int64)]
 
 
 def _fn():
