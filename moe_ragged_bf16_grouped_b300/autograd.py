@@ -18,10 +18,12 @@ convention that the MoE grouped GEMM pull request adopts for the deterministic w
   ``grad_added_to_main_grad`` (which it sets to True; zeros when ``w.zero_out_wgrad`` is true,
   else uninitialised), and None otherwise;
 - ``create_graph`` (a differentiable backward), ``torch.jit.trace`` and ``torch.compile`` raise
-  NotImplementedError.
+  NotImplementedError;
+- a reentrant activation checkpoint (``torch.utils.checkpoint`` with ``use_reentrant=True``)
+  raises ValueError when its forward first runs the fused op; non-reentrant and nested
+  non-reentrant checkpoints work like any autograd graph (the backward adds once).
 
-Without fusion, w's gradient is dW in w's dtype (bf16).  Reentrant activation checkpointing is
-not detected (the pages refuse it); non-reentrant checkpointing works like any autograd graph.
+Without fusion, w's gradient is dW in w's dtype (bf16), under any checkpoint.
 """
 from __future__ import annotations
 
@@ -45,6 +47,39 @@ def _check_main_grad(w: torch.Tensor) -> torch.Tensor:
     return mg
 
 
+def _reentrant_checkpoint_code():
+    try:
+        from torch.utils.checkpoint import CheckpointFunction
+    except ImportError:   # a torch without the reentrant checkpoint function
+        return ()
+    return (CheckpointFunction.forward.__code__, CheckpointFunction.backward.__code__)
+
+
+def _in_reentrant_checkpoint() -> bool:
+    """True when called (at any depth) from the reentrant checkpoint's forward or its
+    recomputing backward."""
+    codes = _reentrant_checkpoint_code()
+    f = sys._getframe(1)
+    while f is not None:
+        if f.f_code in codes:
+            return True
+        f = f.f_back
+    return False
+
+
+def _in_checkpoint_recompute() -> bool:
+    """True while a non-reentrant checkpoint recomputes its forward inside a backward (its
+    saved-tensor unpack hook re-runs the function; the inputs there are recomputed aliases)."""
+    f = sys._getframe(1)
+    while f is not None:
+        c = f.f_code
+        if c.co_name in ("recompute_fn", "unpack_hook") and \
+                c.co_filename.replace("\\", "/").endswith("torch/utils/checkpoint.py"):
+            return True
+        f = f.f_back
+    return False
+
+
 def _refuse_tracing():
     if torch.jit.is_tracing() or torch.compiler.is_compiling():
         raise NotImplementedError("grouped_det_mm cannot be traced or compiled")
@@ -60,10 +95,22 @@ class GroupedDetMm(torch.autograd.Function):
             raise ValueError("fuse_wgrad_accumulation must be a bool")
         _refuse_tracing()
         if fuse_wgrad_accumulation:
-            _check_main_grad(w)
+            if _in_reentrant_checkpoint():
+                raise ValueError("fuse_wgrad_accumulation=True cannot run under a reentrant "
+                                 "activation checkpoint; use use_reentrant=False")
+            # A checkpoint's recomputation only regenerates saved tensors for the node recorded
+            # by the first forward (whose weight object the backward uses); its w is an alias
+            # without main_grad.
+            if not (getattr(w, "main_grad", None) is None and _in_checkpoint_recompute()):
+                _check_main_grad(w)
         y = _gdg.grouped_det_gemm_fwd(x, w, offs)
         ctx.save_for_backward(x, w, offs)
         ctx.fuse = fuse_wgrad_accumulation
+        # The fused backward reads main_grad (and sets grad_added_to_main_grad) on the weight
+        # object itself: under a non-reentrant checkpoint the saved w comes back as a
+        # recomputed alias without those attributes.  w's own history lies upstream of this
+        # node, so holding it here makes no reference cycle.
+        ctx.weight = w if fuse_wgrad_accumulation else None
         return y
 
     @staticmethod
@@ -77,11 +124,12 @@ class GroupedDetMm(torch.autograd.Function):
             dx = _gdg.grouped_det_gemm_dgrad(dy, w, offs)
         if ctx.needs_input_grad[1]:
             if ctx.fuse:
-                mg = _check_main_grad(w)
+                wp = ctx.weight
+                mg = _check_main_grad(wp)
                 _gdg.grouped_det_gemm_wgrad(dy, x, offs, out=mg, accumulate=True)
-                if hasattr(w, "grad_added_to_main_grad"):
-                    w.grad_added_to_main_grad = True
-                    if getattr(w, "zero_out_wgrad", False):
+                if hasattr(wp, "grad_added_to_main_grad"):
+                    wp.grad_added_to_main_grad = True
+                    if getattr(wp, "zero_out_wgrad", False):
                         dw = torch.zeros(w.shape, dtype=w.dtype, device=w.device)
                     else:
                         dw = torch.empty(w.shape, dtype=w.dtype, device=w.device)

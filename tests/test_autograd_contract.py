@@ -2,7 +2,9 @@
 torch stand-ins (test-only), so the routing and the Megatron main_grad convention are checked
 without a GPU: gradients routed to x and w, the fused accumulation into w.main_grad, the
 placeholder and zero_out_wgrad, repeated backwards adding again, autograd.grad without w, a
-frozen w, and the refusals (create_graph, tracing or compiling, bad flag, bad main_grad)."""
+frozen w, activation checkpoints (reentrant refused with the fused accumulation, non-reentrant
+and nested adding once), and the refusals (create_graph, tracing or compiling, bad flag, bad
+main_grad)."""
 import pytest
 import torch
 
@@ -130,3 +132,47 @@ def test_tracing_and_compiling_refused(standins, monkeypatch):
     monkeypatch.setattr(torch.compiler, "is_compiling", lambda: True)
     with pytest.raises(NotImplementedError):
         gdg.grouped_det_mm(x, w, offs)
+
+
+def test_reentrant_checkpoint_refused_with_fusion(standins):
+    from torch.utils.checkpoint import checkpoint
+    x, w, offs, dy = _inputs()
+    w.main_grad = torch.zeros(E, N, K)
+    with pytest.raises(ValueError, match="reentrant"):
+        checkpoint(lambda a, b: gdg.grouped_det_mm(a, b, offs, fuse_wgrad_accumulation=True),
+                   x, w, use_reentrant=True)
+    assert torch.equal(w.main_grad, torch.zeros(E, N, K))
+    # without fusion a reentrant checkpoint is an ordinary recomputation
+    y = checkpoint(lambda a, b: gdg.grouped_det_mm(a, b, offs), x, w, use_reentrant=True)
+    y.backward(dy)
+    assert torch.equal(x.grad, _dgrad(dy, w.detach(), offs))
+    assert torch.equal(w.grad, _wgrad(dy, x.detach(), offs))
+
+
+@pytest.mark.parametrize("nested", [False, True])
+def test_non_reentrant_checkpoint_adds_once(standins, nested):
+    from torch.utils.checkpoint import checkpoint
+    x, w, offs, dy = _inputs()
+    w.main_grad = torch.ones(E, N, K)
+
+    def inner(a, b):
+        return gdg.grouped_det_mm(a, b, offs, fuse_wgrad_accumulation=True)
+
+    def outer(a, b):
+        return checkpoint(inner, a, b, use_reentrant=False) if nested else inner(a, b)
+
+    y = checkpoint(outer, x, w, use_reentrant=False)
+    y.backward(dy)
+    dw = _wgrad(dy, x.detach(), offs, out_dtype=torch.float32)
+    assert torch.equal(w.main_grad, torch.ones(E, N, K) + dw)
+    assert torch.equal(x.grad, _dgrad(dy, w.detach(), offs))
+    assert w.grad is None
+
+
+def test_missing_main_grad_refused_in_checkpointed_forward(standins):
+    """The recomputation exemption does not reach the first forward of a checkpoint."""
+    from torch.utils.checkpoint import checkpoint
+    x, w, offs, _ = _inputs()
+    with pytest.raises(ValueError, match="main_grad"):
+        checkpoint(lambda a, b: gdg.grouped_det_mm(a, b, offs, fuse_wgrad_accumulation=True),
+                   x, w, use_reentrant=False)
