@@ -75,8 +75,9 @@ typedef enum gdg_status {
                            N and K need not be multiples of the 256-wide tiles: the docs
                            page's stable-API rule (N % 256, K % 64) is relaxed, with rows and
                            columns past N or K read as zeros and never written */
-    GDG_EOVERLAP = 3,   /* out shares a byte with an input or the offsets (the accumulate
-                           checks of the MoE grouped GEMM pull request) */
+    GDG_EOVERLAP = 3,   /* out shares a byte with an input, the offsets or the workspace (the
+                           accumulate checks of the MoE grouped GEMM pull request), or two
+                           elements of a strided out share memory */
     GDG_EWORKSPACE = 4, /* workspace missing or smaller than grouped_det_gemm_workspace_bytes */
     GDG_ECUDA = 5,      /* a CUDA runtime or driver call failed (launch, tensor map encode) */
     GDG_ETIMEOUT = 6    /* reported by gdg_device_error(): an in-kernel wait ran out */
@@ -113,9 +114,10 @@ typedef enum gdg_op { GDG_OP_FWD = 0, GDG_OP_DGRAD = 1, GDG_OP_WGRAD = 2 } gdg_o
  * fwd / dgrad is at out[row * out_ld + col], element (e, n, k) of wgrad at
  * out[e * out_es + n * out_ld + k]; 0 means the dense value (N or K for out_ld,
  * N * out_ld for out_es).  Each stride times the element size must be a multiple of 16
- * bytes (GDG_EALIGN), and no two output elements may share memory (GDG_EOVERLAP: rows of
- * out_ld < columns, or experts whose row ranges interleave or overlap).  Inputs (a, b) are
- * always dense.
+ * bytes (GDG_EALIGN), and no two output elements may share memory (GDG_EOVERLAP), checked
+ * as: taking the row and expert dimensions in increasing order of stride, each stride is at
+ * least the span of everything below it (so a permuted [N, E, K] buffer is accepted, rows
+ * shorter than a row's columns are not).  Inputs (a, b) are always dense.
  */
 typedef struct gdg_args {
     const void* a;

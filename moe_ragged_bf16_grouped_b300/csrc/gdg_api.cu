@@ -581,7 +581,7 @@ const char* gdg_status_string(gdg_status status) {
         case GDG_OK: return "ok";
         case GDG_EINVAL: return "invalid argument";
         case GDG_EALIGN: return "shape or alignment rule violated (N % 8, K % 8, 16-byte pointers)";
-        case GDG_EOVERLAP: return "output overlaps an input, the offsets or the workspace";
+        case GDG_EOVERLAP: return "output overlaps itself, an input, the offsets or the workspace";
         case GDG_EWORKSPACE: return "workspace missing or too small";
         case GDG_ECUDA: return "CUDA call failed";
         case GDG_ETIMEOUT: return "an in-kernel wait ran out";
