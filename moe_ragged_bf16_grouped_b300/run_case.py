@@ -6,6 +6,12 @@
 ``--experts`` keeps only the first E groups of the workload's routing (a smaller
 case of the same shapes, e.g. for profiler captures).  Times are CUDA-event
 medians on the launching stream with a 512 MiB L2 flush before each launch.
+
+The JSON line also carries the op's roofline: algorithmic FLOPs 2 M N K and bytes
+(fwd / dgrad: 2 (M K + E_ne N K + M N) with E_ne the non-empty groups; wgrad:
+2 (M K + M N) + E N K s_out, plus E N K s_out read when accumulating),
+t_roof = max(FLOPs / P, bytes / BW) against the measured burst bf16 GEMM rate P
+and copy bandwidth BW of MEASURED_PEAKS.json (when present), and t_roof / t.
 """
 from __future__ import annotations
 
@@ -48,7 +54,7 @@ def main():
     flops = 2.0 * M * w.N * w.K
     ops_in_cfg = " ".join(w.ops)
     fp32 = args.out_dtype == "fp32" or (args.out_dtype is None and "fp32" in ops_in_cfg)
-    acc = args.accumulate or (args.out_dtype is None and "acc" in ops_in_cfg)
+    acc = args.op == "wgrad" and (args.accumulate or (args.out_dtype is None and "acc" in ops_in_cfg))
     if args.op == "fwd":
         out = torch.empty((rows, w.N), dtype=torch.bfloat16, device=dev)
         fn = lambda: gdg.grouped_det_gemm_fwd(d["X"], d["W"], d["offs"], out=out)  # noqa: E731
@@ -80,10 +86,29 @@ def main():
     if gdg.gdg_device_error() != 0:
         raise RuntimeError("device error word set")
     med = float(np.median(ts)) if ts else float("nan")
-    print(json.dumps({"workload": w.name, "op": args.op, "E": w.E, "N": w.N, "K": w.K,
-                      "rows": M, "ms_median": med, "ms_min": float(np.min(ts)) if ts else None,
-                      "tflops": flops / med / 1e9 if ts else None,
-                      "out_dtype": str(out.dtype), "accumulate": acc}))
+    line = {"workload": w.name, "op": args.op, "E": w.E, "N": w.N, "K": w.K,
+            "rows": M, "ms_median": med, "ms_min": float(np.min(ts)) if ts else None,
+            "tflops": flops / med / 1e9 if ts else None,
+            "out_dtype": str(out.dtype), "accumulate": acc}
+    e_ne = int(np.count_nonzero(sizes))
+    if args.op == "wgrad":
+        s_out = out.element_size()
+        nbytes = 2 * (M * w.K + M * w.N) + w.E * w.N * w.K * s_out * (2 if acc else 1)
+    else:
+        nbytes = 2 * (M * w.K + e_ne * w.N * w.K + M * (w.N if args.op == "fwd" else w.K))
+    line["bytes"] = nbytes
+    line["gbs"] = nbytes / med / 1e6 if ts else None
+    peaks_path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                              "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        with open(peaks_path) as f:
+            pk = json.load(f)
+        t_f = flops / (pk["bf16_tflops"] * 1e12) * 1e3
+        t_b = nbytes / (pk["hbm_gbs"] * 1e9) * 1e3
+        line["t_roof_ms"] = max(t_f, t_b)
+        line["roof_bound"] = "tensor" if t_f >= t_b else "hbm"
+        line["frac_of_roof"] = max(t_f, t_b) / med if ts else None
+    print(json.dumps(line))
 
 
 if __name__ == "__main__":
