@@ -188,6 +188,16 @@ typedef struct gdg_plan gdg_plan;
 GDG_API gdg_status gdg_plan_create(int op, const gdg_args* args, const int32_t* offs, int E, int N,
                                    int K, gdg_dtype out_dtype, int accumulate, gdg_plan** plan);
 
+/* TEST ONLY (the pages have no counterpart; it exists to test failure detection without a GPU
+ * fault): launches the call like grouped_det_gemm_<op> (op = GDG_OP_*), except that the first
+ * pipeline stage of CTA pair 0 is armed but never filled.  That pair's bounded waits run out
+ * after about 2 s, it aborts cleanly (in-flight copies and MMAs drain, TMEM is freed) and
+ * gdg_device_error() then reports GDG_ETIMEOUT; the other pairs finish normally, the context
+ * stays usable, and out holds unspecified values.  Never use it for results. */
+GDG_API gdg_status gdg_test_withhold_first_stage(int op, const gdg_args* args, const int32_t* offs,
+                                                 int E, int N, int K, gdg_dtype out_dtype,
+                                                 int accumulate, void* stream);
+
 /* NULL plan: GDG_EINVAL.  A launch failure: GDG_ECUDA. */
 GDG_API gdg_status gdg_plan_launch(const gdg_plan* plan, void* stream);
 

@@ -569,6 +569,16 @@ gdg_status gdg_plan_create(int op, const gdg_args* args, const int32_t* offs, in
     return GDG_OK;
 }
 
+gdg_status gdg_test_withhold_first_stage(int op, const gdg_args* args, const int32_t* offs,
+                                         int E, int N, int K, gdg_dtype out_dtype,
+                                         int accumulate, void* stream) {
+    Plan pl;
+    const gdg_status st = make_plan(op, args, offs, E, N, K, out_dtype, accumulate, &pl);
+    if (st != GDG_OK) return st;
+    pl.p.test_withhold = 1;
+    return launch_plan(pl, static_cast<cudaStream_t>(stream));
+}
+
 gdg_status gdg_plan_launch(const gdg_plan* plan, void* stream) {
     if (!plan) return GDG_EINVAL;
     return launch_plan(plan->pl, static_cast<cudaStream_t>(stream));

@@ -109,6 +109,7 @@ struct GemmParams {
     int offs_kind;
     int split_rows;         // wgrad: > 0 selects the split form
     int max_units;          // units at or past this index are skipped
+    int test_withhold;      // test only: pair 0's even CTA arms its first stage but copies nothing
     int prefetch;           // wgrad accumulate: tmPre is valid
     int64_t ld_out;         // out row stride (elements)
     int64_t es_out;         // wgrad: out expert stride (elements)
@@ -541,6 +542,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     uint8_t* b = a + kABytes;
                     const uint32_t fb = full0 + stage * 8u;
                     if (even) mbar_arrive_expect_tx(&c->full[stage], bytes);
+                    // Failure-detection test: the stage's barrier never completes, so the MMA
+                    // issuer's bounded wait runs out and the pair aborts.
+                    if (p.test_withhold && pair == 0 && even && u == pair && kb == 0) {
+                        if (++stage == R::kStages) { stage = 0; phase ^= 1u; }
+                        continue;
+                    }
                     // Two copies per operand and stage, one per 64-column block, landing as
                     // consecutive sub-tiles.  Columns and rows past a tensor's extent read as
                     // zeros, so N and K need not be multiples of the tile (every x coordinate

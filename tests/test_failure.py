@@ -1,0 +1,73 @@
+"""Failure detection on the GPU without a GPU fault.
+
+The test-only entry point gdg_test_withhold_first_stage launches a normal call except that CTA
+pair 0 arms its first pipeline stage and never fills it (a flag that nothing sets).  The pair's
+bounded waits run out after about 2 s, it aborts cleanly and the library's device error word
+reports GDG_ETIMEOUT; the host reads it after the launch.  The context must stay usable: the
+same call without the hook then matches the oracle, with no error recorded.  No trap, device
+assert, bad address or endless loop is involved.
+"""
+import ctypes
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from helpers import assert_bf16_close, assert_fp32_close, group_rows_mask, inputs_on
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+GDG_ETIMEOUT = 6
+
+
+def withhold(gdg, op_code, args, dims, offs):
+    f = gdg._lib.gdg_test_withhold_first_stage
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int, ctypes.POINTER(gdg.GdgArgs), ctypes.c_void_p] + \
+        [ctypes.c_int] * 5 + [ctypes.c_void_p]
+    return f(op_code, ctypes.byref(args), offs.data_ptr(), *dims,
+             torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.parametrize("op", ["fwd", "wgrad"])
+def test_withheld_stage_times_out_and_context_survives(cuda_lib, op):
+    w = wl.Workload("withhold", E=4, N=512, K=320, ops=(), main_grad_std=1.0)
+    h, d = inputs_on(w, DEV, seed=4, sizes=[300, 0, 77, 513], kind=wl.OFFS_ENDS)
+    kind = h["kind"]
+    assert cuda_lib.gdg_device_error() == 0   # nothing left over from earlier tests
+    if op == "fwd":
+        args, dims, _, keep = cuda_lib._fwd_args(d["X"], d["W"], d["offs"], None, kind)
+        code = cuda_lib.GDG_OP_FWD
+    else:
+        args, dims, _, keep = cuda_lib._wgrad_args(d["G"], d["X"], d["offs"], None, torch.float32,
+                                                   None, False, -1, None, kind)
+        code = cuda_lib.GDG_OP_WGRAD
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    assert withhold(cuda_lib, code, args, dims, d["offs"]) == 0
+    torch.cuda.synchronize()
+    waited = time.monotonic() - t0
+    del keep
+    assert cuda_lib.gdg_device_error() == GDG_ETIMEOUT
+    assert cuda_lib.gdg_device_error() == 0          # read and cleared
+    assert 1.0 < waited < 60.0, waited               # the 2 s in-kernel limit, then a clean exit
+
+    # The context is still usable: the same call without the hook is correct.
+    if op == "fwd":
+        rows = h["rows"]
+        mask = group_rows_mask(h["offs_np"], kind, w.E, rows)
+        Y = cuda_lib.grouped_det_gemm_fwd(d["X"], d["W"], d["offs"], offs_kind=kind)
+        ref = oracle.fwd(h["X"], h["W"], h["offs_np"], kind)
+        assert_bf16_close(Y[torch.from_numpy(mask).to(DEV)], ref[mask], "fwd after abort")
+    else:
+        dW = cuda_lib.grouped_det_gemm_wgrad(d["G"], d["X"], d["offs"], out_dtype=torch.float32,
+                                             split_rows=-1, offs_kind=kind)
+        ref = oracle.wgrad(h["G"], h["X"], h["offs_np"], w.E, kind)
+        assert_fp32_close(dW, ref, "wgrad after abort")
+    torch.cuda.synchronize()
+    assert cuda_lib.gdg_device_error() == 0
+    assert np.isfinite(waited)
