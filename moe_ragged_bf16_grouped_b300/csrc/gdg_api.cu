@@ -109,16 +109,16 @@ struct DeviceInfo {
 
 DeviceInfo g_dev[kMaxDevices];
 
-// Sets the kernel's shared-memory size and finds how many CTA pairs fit on the device at
-// once (the persistent grid).  The grid size never changes results, only speed.
+// Sets the kernel's shared-memory size and lowers *pairs to the number of CTA pairs of it
+// that fit on the device at once (the persistent grid; every variant launches with the
+// smallest).  The grid size never changes results, only speed.
 template <int OP, int EPI, int RT>
 cudaError_t set_up_kernel(int sms, int* pairs) {
     cudaError_t e = cudaFuncSetAttribute(gdg::grouped_gemm_kernel<OP, EPI, RT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(gdg::kGemmSmemBytes));
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
     cfg.blockDim = dim3(gdg::kThreads, 1, 1);
     cfg.dynamicSmemBytes = gdg::kGemmSmemBytes;
@@ -135,7 +135,7 @@ cudaError_t set_up_kernel(int sms, int* pairs) {
         cudaGetLastError();
         n = sms / 2;
     }
-    *pairs = n;
+    if (n < *pairs) *pairs = n;
     return cudaSuccess;
 }
 
@@ -156,6 +156,7 @@ DeviceInfo* device_info(gdg_status* st) {
     std::lock_guard<std::mutex> lock(d.mu);
     if (!d.ready.load(std::memory_order_relaxed)) {
         void* err = nullptr;
+        d.pairs = 1 << 20;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaGetSymbolAddress(&err, g_device_error) != cudaSuccess ||
             set_up_kernel<gdg::OP_FWD, gdg::EPI_BF16, 256>(d.sms, &d.pairs) != cudaSuccess ||
