@@ -61,7 +61,6 @@ constexpr int kMaxStages = 4;
 // wgrad always uses RT = 256 (its B half is 128 columns of X).
 template <int RT>
 struct Ring {
-    static constexpr int kRowTile = RT;
     static constexpr int kStages = RT == 256 ? 3 : 4;
     static constexpr int kBBytes = (RT / 2) * kBK * 2;      // this CTA's half of B
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -126,7 +125,6 @@ struct SmemCtl {
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
-    int total;
     int warp_tot[kThreads / 32];
 };
 
