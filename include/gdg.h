@@ -198,6 +198,12 @@ GDG_API gdg_status gdg_test_withhold_first_stage(int op, const gdg_args* args, c
                                                  int E, int N, int K, gdg_dtype out_dtype,
                                                  int accumulate, void* stream);
 
+/* TEST ONLY (no counterpart on the pages): calls and plans made after it use at most `pairs`
+ * CTA pairs per launch (0 or less: the device's full persistent grid again).  Process-wide and
+ * not synchronised with launches in flight on other threads.  It exists to test that results
+ * do not depend on the grid size; it changes only speed. */
+GDG_API void gdg_test_set_max_pairs(int pairs);
+
 /* NULL plan: GDG_EINVAL.  A launch failure: GDG_ECUDA. */
 GDG_API gdg_status gdg_plan_launch(const gdg_plan* plan, void* stream);
 

@@ -231,7 +231,12 @@ int tiles_per_expert(int N, int K) {
 }
 
 // Persistent grid: two CTAs per pair, at most one pair per unit.
+// Test-only cap on the pairs of a launch (0: none), set by gdg_test_set_max_pairs.
+std::atomic<int> g_max_pairs{0};
+
 int pair_grid(int64_t units, int pairs) {
+    const int cap = g_max_pairs.load(std::memory_order_relaxed);
+    if (cap > 0 && pairs > cap) pairs = cap;
     const int64_t n = units < pairs ? units : pairs;
     return static_cast<int>(2 * (n > 0 ? n : 1));
 }
@@ -579,6 +584,8 @@ gdg_status gdg_test_withhold_first_stage(int op, const gdg_args* args, const int
     pl.p.test_withhold = 1;
     return launch_plan(pl, static_cast<cudaStream_t>(stream));
 }
+
+void gdg_test_set_max_pairs(int pairs) { g_max_pairs.store(pairs > 0 ? pairs : 0); }
 
 gdg_status gdg_plan_launch(const gdg_plan* plan, void* stream) {
     if (!plan) return GDG_EINVAL;
