@@ -13,8 +13,10 @@
  *   dgrad  dX[s_e:t_e] = G[s_e:t_e] @ W[e]      G [rows,N], W [E,N,K] -> dX [rows,K] bf16
  *   wgrad  dW[e]       = G[s_e:t_e]^T @ X[s_e:t_e]  G, X             -> dW [E,N,K] bf16 or fp32
  *
- * All operands are bf16, row-major and contiguous (last dimension has unit
- * stride, rows are packed).  Products accumulate in fp32 on the tensor cores
+ * All inputs are bf16, row-major and dense; outputs are row-major with unit
+ * stride along the last dimension and may be strided views (out_ld, out_es
+ * below).  N and K are multiples of 8 (16-byte rows for the TMA copies);
+ * neither needs to be a multiple of a tile.  Products accumulate in fp32 on the tensor cores
  * and every reduction runs in a fixed order with no atomics, so results are
  * bitwise identical from run to run and independent of the GPU's SM count.
  * An empty group gives a weight gradient of exactly +0.0.
