@@ -40,7 +40,9 @@
  *
  * Ownership: the caller owns every buffer (operands, out, offsets,
  * workspace).  The library allocates no device memory, never synchronises
- * the host, and launches only on the given stream.  Calls are stateless and
+ * the host, and launches only on the given stream.  Every buffer and the
+ * stream belong to the calling thread's current device (cudaSetDevice); the
+ * tensor maps, the device error word and the launch all use that device.  Calls are stateless and
  * may be captured in a CUDA graph; every launch or replay with accumulate
  * adds again.  New offsets or values written into the same buffers are
  * honoured by the next launch.
@@ -69,7 +71,8 @@ extern "C" {
 
 typedef enum gdg_status {
     GDG_OK = 0,
-    GDG_EINVAL = 1,     /* null pointer, E outside [1, GDG_MAX_EXPERTS], N/K <= 0, rows < 0,
+    GDG_EINVAL = 1,     /* null pointer, E outside [1, GDG_MAX_EXPERTS], N/K <= 0, rows outside
+                           [0, GDG_MAX_ROWS],
                            bad dtype or offs_kind, fwd/dgrad with fp32 out or accumulate,
                            bad split_rows */
     GDG_EALIGN = 2,     /* N % 8 or K % 8 != 0 (every operand row must start on a 16-byte
@@ -92,6 +95,10 @@ typedef enum gdg_offs_kind { GDG_OFFS_ENDS = 0, GDG_OFFS_INDPTR = 1 } gdg_offs_k
 typedef enum gdg_op { GDG_OP_FWD = 0, GDG_OP_DGRAD = 1, GDG_OP_WGRAD = 2 } gdg_op;
 
 #define GDG_MAX_EXPERTS 1024
+
+/* Largest rows a call takes (2^31 - 1024): every row coordinate a kernel forms, up to a tile
+ * past the last row, stays inside the int32 range of the TMA copies. */
+#define GDG_MAX_ROWS 2147482624LL
 
 /*
  * Per-call buffers (all device pointers, 16-byte aligned):
@@ -167,6 +174,17 @@ GDG_API const char* gdg_status_string(gdg_status status);
  * GDG_ETIMEOUT) and clears it. */
 GDG_API gdg_status gdg_device_error(void);
 
+/* The device error word without a host synchronisation: enqueues on `stream` (a
+ * cudaStream_t of the current device) a 4-byte copy of the word into *dst, then a reset of
+ * the word to 0.  dst is device memory or pinned (page-locked) host memory of 4 bytes; once
+ * the stream has reached the copy, *dst holds GDG_OK (0) or GDG_ETIMEOUT (6), covering every
+ * launch of this device that completed before it.  Nothing is allocated and the call may be
+ * captured in a CUDA graph.  Returns GDG_EINVAL for a NULL dst, GDG_ECUDA if enqueueing fails.
+ *
+ * A pair of CTAs whose wait ran out (GDG_ETIMEOUT) stopped early: the outputs of that launch
+ * are unspecified and must not be used. */
+GDG_API gdg_status gdg_device_error_async(unsigned int* dst, void* stream);
+
 /*
  * Prepared launches (docs page, "Prepared launches": validate and bind once, then launch any
  * number of times).  gdg_plan_create runs every check of the matching entry point
@@ -231,11 +249,14 @@ GDG_API void gdg_plan_destroy(gdg_plan* plan);
  * for grouped_det_gemm_wgrad; args->workspace and args->workspace_bytes are ignored.
  *
  * It always runs the split form: args->split_rows > 0 (a multiple of 64) is used as given;
- * 0 takes the automatic value, or one chunk per group when the automatic rule picks the
- * unsplit form; a negative value is refused with GDG_EINVAL.  A problem whose partials need
- * more than GDG_NOALLOC_SCRATCH_BYTES (grouped_det_gemm_workspace_bytes for the resolved
- * split_rows) is refused with GDG_EWORKSPACE and nothing is launched.  Results are bitwise
- * equal to grouped_det_gemm_wgrad with the same split_rows.
+ * 0 takes the automatic value (grouped_det_gemm_auto_split_rows) when its partials fit in
+ * the scratch, and otherwise the smallest multiple of 64 whose partials fit (partial tiles:
+ * ceil(N/256) * ceil(K/256) * (ceil(rows / split_rows) + E), 256 KiB each, at most 64); a
+ * negative value is refused with GDG_EINVAL.  A problem whose partials cannot fit
+ * (grouped_det_gemm_workspace_bytes for the given or resolved split_rows above
+ * GDG_NOALLOC_SCRATCH_BYTES, or ceil(N/256) * ceil(K/256) * (E + 1) > 64) is refused with
+ * GDG_EWORKSPACE and nothing is launched.  Results are bitwise equal to
+ * grouped_det_gemm_wgrad with the same (resolved) split_rows.
  *
  * The first call on a device looks up the array's device address (once per device, with
  * that device current); make that first call before any stream capture.  Every call shares

@@ -28,7 +28,7 @@ __all__ = [
     "grouped_det_gemm_wgrad_noalloc", "GDG_NOALLOC_SCRATCH_BYTES", "GroupedDetGemmPlan",
     "prepare_grouped_det_gemm_fwd", "prepare_grouped_det_gemm_dgrad",
     "prepare_grouped_det_gemm_wgrad", "grouped_det_mm", "GroupedDetMm",
-    "gdg_status_string", "gdg_device_error", "library_path",
+    "gdg_status_string", "gdg_device_error", "gdg_device_error_async", "library_path",
 ]
 
 GDG_OK, GDG_EINVAL, GDG_EALIGN, GDG_EOVERLAP, GDG_EWORKSPACE, GDG_ECUDA, GDG_ETIMEOUT = range(7)
@@ -68,6 +68,8 @@ _lib.gdg_status_string.restype = ctypes.c_char_p
 _lib.gdg_status_string.argtypes = [ctypes.c_int]
 _lib.gdg_device_error.restype = ctypes.c_int
 _lib.gdg_device_error.argtypes = []
+_lib.gdg_device_error_async.restype = ctypes.c_int
+_lib.gdg_device_error_async.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
 _lib.gdg_plan_create.restype = ctypes.c_int
 _lib.gdg_plan_create.argtypes = [ctypes.c_int, ctypes.POINTER(GdgArgs), ctypes.c_void_p,
                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -95,6 +97,23 @@ def gdg_status_string(status: int) -> str:
 def gdg_device_error() -> int:
     """Synchronises the device and returns (and clears) the device error word."""
     return _lib.gdg_device_error()
+
+
+def gdg_device_error_async(dst: torch.Tensor, stream=None) -> torch.Tensor:
+    """Enqueues on ``stream`` a copy of the device error word into ``dst`` (one int32 element,
+    on the device or in pinned host memory) and a reset of the word, with no host
+    synchronisation.  Once the stream has passed that point ``dst`` holds 0 (GDG_OK) or 6
+    (GDG_ETIMEOUT: a launch stopped early and its outputs are unspecified)."""
+    if not isinstance(dst, torch.Tensor) or dst.dtype != torch.int32 or dst.numel() < 1:
+        raise ValueError("dst must be an int32 tensor with at least one element")
+    if not dst.is_cuda and not dst.is_pinned():
+        raise ValueError("dst must be on the device or in pinned host memory")
+    device = dst.device if dst.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(device):
+        st = _lib.gdg_device_error_async(dst.data_ptr(), _stream_ptr(stream, device))
+    if st != GDG_OK:
+        raise GdgError(st, "gdg_device_error_async")
+    return dst
 
 
 def grouped_det_gemm_workspace_bytes(op: int, rows: int, E: int, N: int, K: int,
@@ -155,6 +174,13 @@ def _out_strides(out: torch.Tensor):
     return ld, es
 
 
+def _same_device(*tensors):
+    dev = tensors[0].device
+    for t in tensors[1:]:
+        if t is not None and t.device != dev:
+            raise ValueError(f"all tensors must be on one device ({dev}, got {t.device})")
+
+
 def _offs_kind(offs_kind) -> int:
     if offs_kind in (GDG_OFFS_ENDS, "ends", "offs"):
         return GDG_OFFS_ENDS
@@ -175,7 +201,9 @@ def _stream_ptr(stream, device) -> int:
 
 
 def _call(fn, name, args, offs, E, N, K, dtype_code, accumulate, stream):
-    st = fn(ctypes.byref(args), offs.data_ptr(), E, N, K, dtype_code, int(accumulate), stream)
+    # The library works on the calling thread's current device: make it the tensors' device.
+    with torch.cuda.device(offs.device):
+        st = fn(ctypes.byref(args), offs.data_ptr(), E, N, K, dtype_code, int(accumulate), stream)
     if st != GDG_OK:
         raise GdgError(st, name)
 
@@ -192,6 +220,7 @@ def _fwd_args(x, w, offs, out, offs_kind):
     _check_out(out, torch.bfloat16, 2)
     if tuple(out.shape) != (x.shape[0], N):
         raise ValueError("out must be [rows, N]")
+    _same_device(offs, x, w, out)
     args = GdgArgs(x.data_ptr(), w.data_ptr(), out.data_ptr(), None, 0, x.shape[0], kind, 0,
                    *_out_strides(out))
     return args, (E, N, K, GDG_BF16, 0), out, (x, w, offs, out)
@@ -209,6 +238,7 @@ def _dgrad_args(g, w, offs, out, offs_kind):
     _check_out(out, torch.bfloat16, 2)
     if tuple(out.shape) != (g.shape[0], K):
         raise ValueError("out must be [rows, K]")
+    _same_device(offs, g, w, out)
     args = GdgArgs(g.data_ptr(), w.data_ptr(), out.data_ptr(), None, 0, g.shape[0], kind, 0,
                    *_out_strides(out))
     return args, (E, N, K, GDG_BF16, 0), out, (g, w, offs, out)
@@ -236,6 +266,7 @@ def _wgrad_args(g, x, offs, out, out_dtype, num_groups, accumulate, split_rows, 
     if tuple(out.shape) != (E, N, K):
         raise ValueError("out must be [E, N, K]")
     code = _dtype_code(out.dtype)
+    _same_device(offs, g, x, out, workspace)
     need = grouped_det_gemm_workspace_bytes(GDG_OP_WGRAD, rows, E, N, K, out.dtype, accumulate,
                                             split_rows)
     if need and workspace is None:
@@ -296,13 +327,16 @@ class GroupedDetGemmPlan:
         self._keep = keep
         self._device = out.device
         h = ctypes.c_void_p()
-        st = _lib.gdg_plan_create(op, ctypes.byref(args), offs.data_ptr(), *dims, ctypes.byref(h))
+        with torch.cuda.device(self._device):
+            st = _lib.gdg_plan_create(op, ctypes.byref(args), offs.data_ptr(), *dims,
+                                      ctypes.byref(h))
         if st != GDG_OK:
             raise GdgError(st, name)
         self._h = h
 
     def launch(self, stream=None) -> torch.Tensor:
-        st = _lib.gdg_plan_launch(self._h, _stream_ptr(stream, self._device))
+        with torch.cuda.device(self._device):
+            st = _lib.gdg_plan_launch(self._h, _stream_ptr(stream, self._device))
         if st != GDG_OK:
             raise GdgError(st, "gdg_plan_launch")
         return self.out
@@ -357,6 +391,7 @@ def grouped_det_gemm_wgrad_noalloc(g: torch.Tensor, x: torch.Tensor, offs: torch
     _check_out(out, out.dtype, 3)
     if tuple(out.shape) != (E, N, K):
         raise ValueError("out must be [E, N, K]")
+    _same_device(offs, g, x, out)
     args = GdgArgs(g.data_ptr(), x.data_ptr(), out.data_ptr(), None, 0, rows, kind, split_rows,
                    *_out_strides(out))
     _call(_lib.grouped_det_gemm_wgrad_noalloc, "grouped_det_gemm_wgrad_noalloc", args, offs, E,

@@ -241,6 +241,25 @@ int pair_grid(int64_t units, int pairs) {
     return static_cast<int>(2 * (n > 0 ? n : 1));
 }
 
+// L2 eviction priorities of a wgrad launch (GemmParams::l2): the output stores go first
+// (nothing re-reads dW); with accumulate, G and X (re-read by every tile of their group) and
+// the output blocks prefetched into L2 stay until they are read.
+uint32_t l2_policy_bits(int accumulate) {
+    using gdg::L2_EVICT_FIRST;
+    using gdg::L2_EVICT_LAST;
+    using gdg::L2_NORMAL;
+    uint32_t a = L2_NORMAL, b = L2_NORMAL, st = L2_EVICT_FIRST, ld = L2_NORMAL;
+    if (accumulate) a = b = ld = L2_EVICT_LAST;
+    return a | (b << 2) | (st << 4) | (ld << 6);
+}
+
+// wgrad, unsplit: walk the groups by decreasing size when groups are long on average (at least
+// 512 rows): the tiles of one group then run side by side and its rows come from HBM once.
+// A rule on shapes only.
+int sort_groups_rule(int64_t rows, int E) {
+    return (E <= gdg::kMaxSorted && rows >= static_cast<int64_t>(E) * 512) ? 1 : 0;
+}
+
 int32_t auto_split_rows(int64_t rows, int E, int N, int K) {
     const int64_t tpe = tiles_per_expert(N, K);
     // Shapes with few output tiles leave SMs idle in the unsplit form; cut the rows of
@@ -262,7 +281,7 @@ gdg_status check_common(const gdg_args* args, const int32_t* offs, int E, int N,
                         gdg_dtype out_dtype) {
     if (!args) return GDG_EINVAL;
     if (E < 1 || E > GDG_MAX_EXPERTS || N <= 0 || K <= 0 || args->rows < 0 ||
-        args->rows > INT32_MAX - 1)
+        args->rows > GDG_MAX_ROWS)
         return GDG_EINVAL;
     if (args->offs_kind != GDG_OFFS_ENDS && args->offs_kind != GDG_OFFS_INDPTR) return GDG_EINVAL;
     if (out_dtype != GDG_BF16 && out_dtype != GDG_FP32) return GDG_EINVAL;
@@ -429,6 +448,8 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
     p.max_units = static_cast<int>(max_units);
     p.ld_out = L.ld;
     p.es_out = L.es;
+    p.l2 = l2_policy_bits(accumulate);
+    p.sort_groups = split ? 0 : sort_groups_rule(rows, E);
     pl->grid = pair_grid(max_units, dev->pairs);
     pl->epi = split ? static_cast<int>(gdg::EPI_PARTIAL) : epi;
     pl->launch = true;
@@ -607,6 +628,20 @@ const char* gdg_status_string(gdg_status status) {
     return "unknown status";
 }
 
+gdg_status gdg_device_error_async(unsigned int* dst, void* stream) {
+    if (!dst) return GDG_EINVAL;
+    gdg_status st = GDG_OK;
+    DeviceInfo* dev = device_info(&st);
+    if (!dev) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(dst, dev->err, sizeof(unsigned int), cudaMemcpyDefault, s) != cudaSuccess ||
+        cudaMemsetAsync(dev->err, 0, sizeof(unsigned int), s) != cudaSuccess) {
+        cudaGetLastError();
+        return GDG_ECUDA;
+    }
+    return GDG_OK;
+}
+
 gdg_status gdg_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return GDG_ECUDA;
     unsigned int v = 0, zero = 0;
@@ -658,20 +693,34 @@ void* noalloc_scratch(gdg_status* st) {
     return p;
 }
 
+// split_rows for the fixed scratch when the caller passes 0: the automatic value if its partials
+// fit, else the smallest multiple of 64 whose partials fit (the most parallel split that does),
+// or -1 when even one chunk per group does not fit.  Partials: tpe * (ceil(rows / s) + E) tiles.
+int32_t noalloc_split_rows(int64_t rows, int E, int N, int K) {
+    const int64_t tpe = tiles_per_expert(N, K);
+    const int64_t tiles = GDG_NOALLOC_SCRATCH_BYTES / (gdg::kPartialElems * sizeof(float));
+    const int64_t chunks = tiles / tpe - E;          // most row chunks whose partials fit
+    if (chunks < 1) return -1;
+    const int32_t a = auto_split_rows(rows, E, N, K);
+    if (a > 0 && ceil_div(rows, a) <= chunks) return a;
+    int64_t s = ceil_div(ceil_div(rows > 0 ? rows : 1, chunks), 64) * 64;
+    if (s > (int64_t{1} << 30)) return -1;
+    return static_cast<int32_t>(s);
+}
+
 }  // namespace
 
 extern "C" gdg_status grouped_det_gemm_wgrad_noalloc(const gdg_args* args, const int32_t* offs,
                                                      int E, int N, int K, gdg_dtype out_dtype,
                                                      int accumulate, void* stream) {
     if (!args || args->split_rows < 0) return GDG_EINVAL;
+    if (E < 1 || E > GDG_MAX_EXPERTS || N <= 0 || K <= 0 || N % 8 || K % 8 || args->rows < 0 ||
+        args->rows > GDG_MAX_ROWS)
+        return GDG_EINVAL;
     int32_t split_rows = args->split_rows;
     if (split_rows == 0) {
-        split_rows = grouped_det_gemm_auto_split_rows(args->rows, E, N, K);
-        if (split_rows <= 0) {   // automatic rule picked the unsplit form: one chunk per group
-            const int64_t r = args->rows > 64 ? args->rows : 64;
-            if (r > (int64_t{1} << 30)) return GDG_EINVAL;
-            split_rows = static_cast<int32_t>((r + 63) / 64 * 64);
-        }
+        split_rows = noalloc_split_rows(args->rows, E, N, K);
+        if (split_rows < 0) return GDG_EWORKSPACE;
     }
     const size_t need = grouped_det_gemm_workspace_bytes(GDG_OP_WGRAD, args->rows, E, N, K,
                                                          out_dtype, accumulate, split_rows);

@@ -77,6 +77,7 @@ constexpr int kTailBufs = 2;
 constexpr int kThreads = 384;               // GEMM kernel: 4 role warps + 8 epilogue warps
 constexpr int kReduceThreads = 256;
 constexpr int kMaxE = 1024;
+constexpr int kMaxSorted = 256;             // wgrad: groups walked by size need E <= this
 constexpr int kTmemCols = 512;
 constexpr int kPartialElems = kPairM * kBN; // fp32 elements per split partial tile
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // any single wait > 2 s is a hang
@@ -112,7 +113,13 @@ struct GemmParams {
     int prefetch;           // wgrad accumulate: tmPre is valid
     int64_t ld_out;         // out row stride (elements)
     int64_t es_out;         // wgrad: out expert stride (elements)
+    uint32_t l2;            // wgrad: L2 eviction priorities (L2Pol): bits [0, 2) A copies,
+                            // [2, 4) B copies, [4, 6) output stores, [6, 8) old-value loads
+                            // and prefetches of the output
+    int sort_groups;        // wgrad, unsplit, E <= kMaxSorted: walk the groups by size
 };
+
+__device__ __forceinline__ int l2_field(uint32_t l2, int i) { return (l2 >> (2 * i)) & 3; }
 
 struct SmemCtl {
     uint64_t full[kMaxStages];  // even CTA: both CTAs' copies of a stage have landed
@@ -125,7 +132,8 @@ struct SmemCtl {
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
-    int warp_tot[kThreads / 32];
+    int64_t warp_tot[kThreads / 32];
+    uint16_t order[kMaxSorted];  // sort_groups: the groups by decreasing size (ties: index)
 };
 
 constexpr size_t kGemmSmemBytes =
@@ -160,13 +168,18 @@ __device__ __forceinline__ void group_range(const int32_t* offs, int kind, int64
     m = static_cast<int>(b - a);
 }
 
+// Units of a group of m rows.  64-bit: with offsets that are not cumulative (several groups
+// clamped to the same rows) the sum over groups can pass the int range, and m + RT - 1 can pass
+// it for m near 2^31.  A single group's count never exceeds max_units (< 2^31), checked on the
+// host.
 template <int OP, int RT>
-__device__ __forceinline__ int units_of_group(int m, const Shape& sh, int split_rows) {
+__device__ __forceinline__ int64_t units_of_group(int m, const Shape& sh, int split_rows) {
     if (OP == OP_WGRAD) {
-        if (split_rows > 0) return ((m + split_rows - 1) / split_rows) * sh.ft;
+        if (split_rows > 0)
+            return ((static_cast<int64_t>(m) + split_rows - 1) / split_rows) * sh.ft;
         return sh.ft;       // every tile of every expert, empty groups included
     }
-    return ((m + RT - 1) / RT) * sh.ft;
+    return ((static_cast<int64_t>(m) + RT - 1) / RT) * sh.ft;
 }
 
 // Builds start/size/prefix/total in shared memory (ordered reduce of split partials).  Every
@@ -174,9 +187,11 @@ __device__ __forceinline__ int units_of_group(int m, const Shape& sh, int split_
 template <int OP>
 __device__ void build_schedule(const int32_t* offs, int kind, int64_t rows, int E,
                                int split_rows, int max_units, const Shape& sh, int* start,
-                               int* size, int* prefix, int* warp_tot, int* total) {
+                               int* size, int* prefix, int64_t* warp_tot, int* total) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int v[4], local = 0;
+    // Each count is capped at max_units (< 2^31), so no 64-bit partial sum below can overflow;
+    // prefixes are capped at max_units again when stored (no unit at or past max_units exists).
+    int64_t v[4], local = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int e = tid * 4 + j;
@@ -186,39 +201,40 @@ __device__ void build_schedule(const int32_t* offs, int kind, int64_t rows, int 
             group_range(offs, kind, rows, e, s, m);
             start[e] = s;
             size[e] = m;
-            v[j] = units_of_group<OP, 256>(m, sh, split_rows);
+            const int64_t n = units_of_group<OP, 256>(m, sh, split_rows);
+            v[j] = n < max_units ? n : max_units;
         }
         local += v[j];
     }
-    int x = local;
+    int64_t x = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
     if (lane == 31) warp_tot[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int t = lane < kReduceThreads / 32 ? warp_tot[lane] : 0;
+        int64_t t = lane < kReduceThreads / 32 ? warp_tot[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            const int64_t y = __shfl_up_sync(0xffffffffu, t, o);
             if (lane >= o) t += y;
         }
         if (lane < kReduceThreads / 32) warp_tot[lane] = t;
     }
     __syncthreads();
-    int base = (warp ? warp_tot[warp - 1] : 0) + x - local;
+    int64_t base = (warp ? warp_tot[warp - 1] : 0) + x - local;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int e = tid * 4 + j;
-        if (e < E) prefix[e] = base;
+        if (e < E) prefix[e] = static_cast<int>(base < max_units ? base : max_units);
         base += v[j];
     }
     if (tid == 0) {
-        const int tot = warp_tot[kReduceThreads / 32 - 1];
-        prefix[E] = tot;
-        *total = tot < max_units ? tot : max_units;
+        const int64_t tot = warp_tot[kReduceThreads / 32 - 1];
+        prefix[E] = static_cast<int>(tot < max_units ? tot : max_units);
+        *total = prefix[E];
     }
     __syncthreads();
 }
@@ -226,9 +242,9 @@ __device__ void build_schedule(const int32_t* offs, int kind, int64_t rows, int 
 // Number of work units over all groups, capped at max_units.  Every thread of the block
 // calls it.
 template <int OP, int RT>
-__device__ int count_units(const GemmParams& p, const Shape& sh, int* warp_tot) {
+__device__ int count_units(const GemmParams& p, const Shape& sh, int64_t* warp_tot) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int local = 0;
+    int64_t local = 0;      // at most 3 groups per thread, each below 2^31 units
     for (int e = tid; e < p.E; e += kThreads) {
         int s, m;
         group_range(p.offs, p.offs_kind, p.rows, e, s, m);
@@ -238,22 +254,47 @@ __device__ int count_units(const GemmParams& p, const Shape& sh, int* warp_tot) 
     for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
     if (lane == 0) warp_tot[warp] = local;
     __syncthreads();
-    int tot = 0;
+    int64_t tot = 0;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) tot += warp_tot[w];
-    return tot < p.max_units ? tot : p.max_units;
+    return static_cast<int>(tot < p.max_units ? tot : p.max_units);
 }
 
-// Walks the groups forward: group e holds units [base, base + n) and rows [s, s + m).
+// Walks the groups forward: the pos-th group of the walk is e (e = pos, or order[pos] when the
+// groups are walked by size); it holds units [base, base + n) and rows [s, s + m).  base and n
+// are 64-bit for the same reason as units_of_group.
 struct Cursor {
-    int e, base, n, s, m;
+    int64_t base, n;
+    int pos, e, s, m;
+    const uint16_t* order;      // nullptr: natural order
 };
 
+// sort_groups: order[] = the groups by decreasing row count, ties by index.  Long groups first
+// and groups of similar length next to each other keep the pairs that share a group's rows
+// (every tile of it) working on them at the same time, so the rows are read from HBM once.
+// Every thread of the block calls it; a later __syncthreads publishes order[].
+__device__ __forceinline__ void sort_groups_by_size(const GemmParams& p, uint16_t* order) {
+    for (int e = threadIdx.x; e < p.E; e += kThreads) {
+        int s, m;
+        group_range(p.offs, p.offs_kind, p.rows, e, s, m);
+        int rank = 0;
+        for (int j = 0; j < p.E; ++j) {
+            int sj, mj;
+            group_range(p.offs, p.offs_kind, p.rows, j, sj, mj);
+            rank += (mj > m || (mj == m && j < e)) ? 1 : 0;
+        }
+        order[rank] = static_cast<uint16_t>(e);
+    }
+}
+
 template <int OP, int RT>
-__device__ __forceinline__ void cursor_init(Cursor& cu, const GemmParams& p, const Shape& sh) {
-    cu.e = 0;
+__device__ __forceinline__ void cursor_init(Cursor& cu, const GemmParams& p, const Shape& sh,
+                                            const uint16_t* order) {
+    cu.order = order;
+    cu.pos = 0;
+    cu.e = order ? order[0] : 0;
     cu.base = 0;
-    group_range(p.offs, p.offs_kind, p.rows, 0, cu.s, cu.m);
+    group_range(p.offs, p.offs_kind, p.rows, cu.e, cu.s, cu.m);
     cu.n = units_of_group<OP, RT>(cu.m, sh, p.split_rows);
 }
 
@@ -262,9 +303,10 @@ __device__ __forceinline__ void cursor_init(Cursor& cu, const GemmParams& p, con
 template <int OP, int RT>
 __device__ __forceinline__ void cursor_seek(Cursor& cu, const GemmParams& p, const Shape& sh,
                                             int u) {
-    while (u >= cu.base + cu.n && cu.e + 1 < p.E) {
+    while (u >= cu.base + cu.n && cu.pos + 1 < p.E) {
         cu.base += cu.n;
-        ++cu.e;
+        ++cu.pos;
+        cu.e = cu.order ? cu.order[cu.pos] : cu.pos;
         group_range(p.offs, p.offs_kind, p.rows, cu.e, cu.s, cu.m);
         cu.n = units_of_group<OP, RT>(cu.m, sh, p.split_rows);
     }
@@ -325,7 +367,7 @@ __device__ __forceinline__ Tile decode_unit(const GemmParams& p, Cursor& cu, con
     Tile t;
     t.u = u;
     t.e = cu.e;
-    const int local = u - cu.base;
+    const int local = static_cast<int>(u - cu.base);   // < cu.n, which fits an int
     const int s = cu.s, m = cu.m;
     if (OP == OP_WGRAD) {
         const int sp = local / sh.ft;
@@ -342,7 +384,7 @@ __device__ __forceinline__ Tile decode_unit(const GemmParams& p, Cursor& cu, con
             t.nred = m;
         }
     } else {
-        const int rc_n = (m + RT - 1) / RT;
+        const int rc_n = static_cast<int>((static_cast<int64_t>(m) + RT - 1) / RT);
         const int ft = local / rc_n, rc = local - ft * rc_n;
         t.f0 = ft * kPairM;
         t.c0 = s + rc * RT;
@@ -478,9 +520,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else
             for (int i = 0; i < 5; ++i) prefetch_tmap(&p.tmB[i]);
     }
-    const int total = count_units<OP, RT>(p, sh, c->warp_tot);
+    const bool sorted = OP == OP_WGRAD && p.sort_groups && p.E <= kMaxSorted;
+    if (sorted) sort_groups_by_size(p, c->order);
+    const int total = count_units<OP, RT>(p, sh, c->warp_tot);   // its __syncthreads publishes order
     Cursor cu;
-    cursor_init<OP, RT>(cu, p, sh);
+    cursor_init<OP, RT>(cu, p, sh, sorted ? c->order : nullptr);
     // Both CTAs' barriers are initialised (and the peer has started) before any CTA signals
     // the other's barriers or allocates TMEM together with it.
     cluster_sync();
@@ -497,6 +541,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- TMA producer (both CTAs)
         if (lane == 0) {
             const uint32_t full0 = mapa_shared(smem_u32(&c->full[0]), 0u);
+            // wgrad only: fwd / dgrad copies and stores take the default L2 policy (eviction
+            // hints measured no faster there).
+            const uint64_t pol_a = make_l2_policy(l2_field(p.l2, 0));
+            const uint64_t pol_b = make_l2_policy(l2_field(p.l2, 1));
+            const uint64_t pol_r = make_l2_policy(l2_field(p.l2, 3));
             int stage = 0, jt = 0;   // jt: units with a tail step so far
             uint32_t phase = 0;
             bool ok = true;
@@ -512,7 +561,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     p.prefetch && fa + kBM <= p.N)
                     // The epilogue reads this CTA's 128 x 256 block of out after the unit's
                     // mainloop: start bringing it into L2 now (whole 128-row blocks only).
-                    tma_prefetch_3d(&p.tmPre, t.c0, fa, t.e);
+                    tma_prefetch_3d(&p.tmPre, t.c0, fa, t.e, pol_r);
                 if (OP == OP_WGRAD) {
                     const int v = tail_rows(t.nred, t.nkb);
                     if (v) {
@@ -527,10 +576,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const int xb = (t.c0 + (kBN / 2) * static_cast<int>(pr.rank));
                         uint8_t* tbuf = tail_area + tb * kTailBytes;
                         mbar_arrive_expect_tx(&c->tb_full[tb], kTailBytes);
-                        tma_load_2d(tbuf, &p.tmTail[0], &c->tb_full[tb], fa, rt0);
-                        tma_load_2d(tbuf + kTailSub, &p.tmTail[0], &c->tb_full[tb], fa + 64, rt0);
-                        tma_load_2d(tbuf + 2 * kTailSub, &p.tmTail[1], &c->tb_full[tb], xb, rt0);
-                        tma_load_2d(tbuf + 3 * kTailSub, &p.tmTail[1], &c->tb_full[tb], xb + 64, rt0);
+                        tma_load_2d(tbuf, &p.tmTail[0], &c->tb_full[tb], fa, rt0, pol_a);
+                        tma_load_2d(tbuf + kTailSub, &p.tmTail[0], &c->tb_full[tb], fa + 64, rt0, pol_a);
+                        tma_load_2d(tbuf + 2 * kTailSub, &p.tmTail[1], &c->tb_full[tb], xb, rt0, pol_b);
+                        tma_load_2d(tbuf + 3 * kTailSub, &p.tmTail[1], &c->tb_full[tb], xb + 64, rt0, pol_b);
                         ++jt;
                     }
                 }
@@ -565,10 +614,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         // 128 reduction rows x this CTA's two 64-wide blocks of G and of X.
                         const int r = t.r0 + kb * kBK;
                         const int xb = t.c0 + (kBN / 2) * static_cast<int>(pr.rank);
-                        tma_load_2d_pair(a, &p.tmA, fb, fa, r);
-                        tma_load_2d_pair(a + kSubBytes, &p.tmA, fb, fa + 64, r);
-                        tma_load_2d_pair(b, &p.tmB[0], fb, xb, r);
-                        tma_load_2d_pair(b + kSubBytes, &p.tmB[0], fb, xb + 64, r);
+                        tma_load_2d_pair(a, &p.tmA, fb, fa, r, pol_a);
+                        tma_load_2d_pair(a + kSubBytes, &p.tmA, fb, fa + 64, r, pol_a);
+                        tma_load_2d_pair(b, &p.tmB[0], fb, xb, r, pol_b);
+                        tma_load_2d_pair(b + kSubBytes, &p.tmB[0], fb, xb + 64, r, pol_b);
                     }
                     if (++stage == R::kStages) { stage = 0; phase ^= 1u; }
                 }
@@ -717,6 +766,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int rr = lane >> 2, gg = lane & 3;        // line-order phase: rows rr + 8j, chunk gg
         uint8_t* wslot = box + lane * 64;               // this lane's row in the write phase
         const int wsw = (lane >> 1) & 3;                // 64-byte swizzle: chunk g at g ^ wsw
+        const uint64_t pol_o = make_l2_policy(l2_field(p.l2, 2));
+        const uint64_t pol_r = make_l2_policy(l2_field(p.l2, 3));
         bool ok = true;
         int nextb = 0;
         Acq acq;                        // the MMA issuer's buffer plan, followed step by step
@@ -764,9 +815,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (b < nbox)
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
-                                old[b][j] = inside(b, j) ? *reinterpret_cast<const uint4*>(
-                                                              gseg + b * 64 + 8 * j * ldo)
-                                                        : make_uint4(0, 0, 0, 0);
+                                old[b][j] = inside(b, j) ? ld_global_v4(gseg + b * 64 + 8 * j * ldo, pol_r)
+                                                         : make_uint4(0, 0, 0, 0);
                 }
             };
             int fb = A;                 // the buffer that ends up holding the unit's value
@@ -872,15 +922,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             v.w = pack_bf16x2(__fadd_rn(bf16_lo(o.w), bf16_lo(v.w)), __fadd_rn(bf16_hi(o.w), bf16_hi(v.w)));
                         }
                     }
-                    if (inside(b, j)) *reinterpret_cast<uint4*>(gline + 8 * j * ldo) = v;
+                    if (inside(b, j)) st_global_v4(gline + 8 * j * ldo, v, pol_o);
                 }
                 if constexpr (acc) {
                     if (b + kAhead < nbox)
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             old[b % kAhead][j] = inside(b + kAhead, j)
-                                                     ? *reinterpret_cast<const uint4*>(
-                                                           gseg + (b + kAhead) * 64 + 8 * j * ldo)
+                                                     ? ld_global_v4(gseg + (b + kAhead) * 64 + 8 * j * ldo, pol_r)
                                                      : make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();   // the box is rewritten by the next box
@@ -969,7 +1018,7 @@ struct ReduceParams {
 };
 
 struct ReduceSmem {
-    int warp_tot[kReduceThreads / 32];
+    int64_t warp_tot[kReduceThreads / 32];
     int total;
     int start[kMaxE];
     int size[kMaxE];
@@ -994,12 +1043,13 @@ __global__ void __launch_bounds__(kReduceThreads) wgrad_reduce_kernel(const __gr
         const int64_t rem = idx - e * NK;
         const int n = static_cast<int>(rem / p.K);
         const int k = static_cast<int>(rem - static_cast<int64_t>(n) * p.K);
-        const int S = (sm.size[e] + p.split_rows - 1) / p.split_rows;
+        const int S = static_cast<int>((static_cast<int64_t>(sm.size[e]) + p.split_rows - 1) / p.split_rows);
         const int tile = (n / kPairM) * sh.kt + k / kBN;
         const size_t within = static_cast<size_t>(n % kPairM) * kBN + (k % kBN);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s = 0; s < S; ++s) {
-            const int u = sm.prefix[e] + s * sh.ft + tile;
+            // prefix <= max_units and s * ft + tile < the group's own count <= max_units.
+            const int64_t u = static_cast<int64_t>(sm.prefix[e]) + static_cast<int64_t>(s) * sh.ft + tile;
             if (u >= p.max_units) break;
             const float4 v = *reinterpret_cast<const float4*>(
                 p.partial + static_cast<size_t>(u) * kPartialElems + within);

@@ -38,12 +38,29 @@ def _fn():
     return f
 
 
+def noalloc_split_rows(rows, E, N, K, auto):
+    """What split_rows = 0 resolves to: the automatic value if its partial tiles fit in the
+    fixed scratch (at most 64 tiles of 256 x 256 fp32), else the smallest multiple of 64 whose
+    tiles fit; None when nothing fits."""
+    tpe = -(-N // 256) * -(-K // 256)
+    chunks = 64 // tpe - E
+    if chunks < 1:
+        return None
+    if auto > 0 and -(-rows // auto) <= chunks:
+        return auto
+    return -(-(-(-max(rows, 1) // chunks)) // 64) * 64
+
+
 def test_refuses_before_any_launch():
     """Refusals happen on the host: no device is touched (fake, aligned addresses)."""
     f = _fn()
     # 1M rows cut into 64-row chunks need far more than the fixed scratch
     big = Args(0x100000, 0x40000000, 0x80000000, None, 0, 1 << 20, 0, 64)
     assert f(ctypes.byref(big), 0xC0000000, 64, 4096, 4096, 1, 0, None) == EWORKSPACE
+    # split_rows = 0 with shapes whose partials cannot fit even one chunk per group
+    # (16 tiles per expert x (4 experts + 1 chunk) > 64 tiles)
+    auto0 = Args(0x100000, 0x40000000, 0x80000000, None, 0, 4096, 0, 0)
+    assert f(ctypes.byref(auto0), 0xC0000000, 4, 1024, 1024, 1, 0, None) == EWORKSPACE
     neg = Args(0x100000, 0x40000000, 0x80000000, None, 0, 512, 0, -1)
     assert f(ctypes.byref(neg), 0xC0000000, 4, 256, 256, 1, 0, None) == EINVAL
     assert f(None, 0xC0000000, 4, 256, 256, 1, 0, None) == EINVAL
@@ -66,19 +83,24 @@ def test_matches_workspace_entry_point_on_two_calls(cuda_lib):
          [300, 0, 1, 17, 513, 255], wl.OFFS_ENDS, 128, False, torch.float32),
         (wl.Workload("t", E=4, N=256, K=256, ops=(), main_grad_std=1.0),
          [200, 0, 311, 1], wl.OFFS_INDPTR, 0, True, torch.float32),
+        # split_rows = 0 where the automatic split's partials do not fit: a coarser split
+        # that fits is chosen (65536 rows, 1 tile per expert: 1152-row chunks, 61 tiles)
+        (wl.Workload("big", E=4, N=256, K=256, ops=(), main_grad_std=1.0),
+         [30000, 0, 35535, 1], wl.OFFS_ENDS, 0, False, torch.bfloat16),
     ]
     for w, sizes, kind, split, acc, dt in cases:     # two calls in a row, different shapes
         _, d = inputs_on(w, "cuda", seed=7, sizes=sizes, kind=kind)
+        resolved0 = split if split > 0 else noalloc_split_rows(
+            d["rows"], w.E, w.N, w.K,
+            cuda_lib.grouped_det_gemm_auto_split_rows(d["rows"], w.E, w.N, w.K))
         need = cuda_lib.grouped_det_gemm_workspace_bytes(
-            cuda_lib.GDG_OP_WGRAD, d["rows"], w.E, w.N, w.K, dt, acc,
-            split if split > 0 else 0)
+            cuda_lib.GDG_OP_WGRAD, d["rows"], w.E, w.N, w.K, dt, acc, resolved0)
         assert 0 < need <= cuda_lib.GDG_NOALLOC_SCRATCH_BYTES
         start = d["main_grad"].to(dt) if acc else torch.full((w.E, w.N, w.K), 9.0,
                                                               dtype=dt, device="cuda")
-        resolved = split if split > 0 else cuda_lib.grouped_det_gemm_auto_split_rows(
-            d["rows"], w.E, w.N, w.K)
-        if resolved <= 0:
-            resolved = (max(d["rows"], 64) + 63) // 64 * 64
+        resolved = split if split > 0 else noalloc_split_rows(
+            d["rows"], w.E, w.N, w.K,
+            cuda_lib.grouped_det_gemm_auto_split_rows(d["rows"], w.E, w.N, w.K))
         ref = cuda_lib.grouped_det_gemm_wgrad(d["G"], d["X"], d["offs"], out=start.clone(),
                                               accumulate=acc, split_rows=resolved,
                                               offs_kind=kind)
@@ -86,5 +108,6 @@ def test_matches_workspace_entry_point_on_two_calls(cuda_lib):
         _call(f, d["G"], d["X"], d["offs"], got, split, acc, kind)
         torch.cuda.synchronize()
         assert cuda_lib.gdg_device_error() == 0
-        assert_fp32_close(got, to64(ref), "no-alloc vs workspace entry point")
-        assert_bitwise(got, ref, "no-alloc vs workspace entry point")
+        if dt == torch.float32:
+            assert_fp32_close(got, to64(ref), "no-alloc vs workspace entry point")
+        assert_bitwise(got, ref, f"no-alloc vs workspace entry point (split_rows {resolved})")
