@@ -241,18 +241,6 @@ int pair_grid(int64_t units, int pairs) {
     return static_cast<int>(2 * (n > 0 ? n : 1));
 }
 
-// L2 eviction priorities of a wgrad launch (GemmParams::l2): the output stores go first
-// (nothing re-reads dW); with accumulate, G and X (re-read by every tile of their group) and
-// the output blocks prefetched into L2 stay until they are read.
-uint32_t l2_policy_bits(int accumulate) {
-    using gdg::L2_EVICT_FIRST;
-    using gdg::L2_EVICT_LAST;
-    using gdg::L2_NORMAL;
-    uint32_t a = L2_NORMAL, b = L2_NORMAL, st = L2_EVICT_FIRST, ld = L2_NORMAL;
-    if (accumulate) a = b = ld = L2_EVICT_LAST;
-    return a | (b << 2) | (st << 4) | (ld << 6);
-}
-
 // wgrad, unsplit: walk the groups by decreasing size when groups are long on average (at least
 // 512 rows): the tiles of one group then run side by side and its rows come from HBM once.
 // A rule on shapes only.
@@ -448,7 +436,6 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
     p.max_units = static_cast<int>(max_units);
     p.ld_out = L.ld;
     p.es_out = L.es;
-    p.l2 = l2_policy_bits(accumulate);
     p.sort_groups = split ? 0 : sort_groups_rule(rows, E);
     pl->grid = pair_grid(max_units, dev->pairs);
     pl->epi = split ? static_cast<int>(gdg::EPI_PARTIAL) : epi;

@@ -113,13 +113,9 @@ struct GemmParams {
     int prefetch;           // wgrad accumulate: tmPre is valid
     int64_t ld_out;         // out row stride (elements)
     int64_t es_out;         // wgrad: out expert stride (elements)
-    uint32_t l2;            // wgrad: L2 eviction priorities (L2Pol): bits [0, 2) A copies,
-                            // [2, 4) B copies, [4, 6) output stores, [6, 8) old-value loads
-                            // and prefetches of the output
     int sort_groups;        // wgrad, unsplit, E <= kMaxSorted: walk the groups by size
 };
 
-__device__ __forceinline__ int l2_field(uint32_t l2, int i) { return (l2 >> (2 * i)) & 3; }
 
 struct SmemCtl {
     uint64_t full[kMaxStages];  // even CTA: both CTAs' copies of a stage have landed
@@ -471,6 +467,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// Descriptor address-field offsets (bytes / 16) of MMA step kk (K = 16) within a stage.
+// K-major operands (fwd A, fwd / dgrad B): 16-element steps are 32 B apart inside a 64-wide
+// block and blocks are a sub-tile apart (A: kSubBytes; B: b_sub).  MN-major operands (dgrad A,
+// wgrad A and B): 16 reduction rows are 2 KB apart.
+template <int OP>
+__device__ __forceinline__ uint64_t a_step(int kk) {
+    return OP == OP_FWD ? static_cast<uint64_t>((kk >> 2) * (kSubBytes >> 4) + (kk & 3) * 2)
+                        : static_cast<uint64_t>(kk * (2048 >> 4));
+}
+
+template <int OP>
+__device__ __forceinline__ uint64_t b_step(int kk, uint32_t b_sub) {
+    return OP == OP_WGRAD ? static_cast<uint64_t>(kk * (2048 >> 4))
+                          : static_cast<uint64_t>((kk >> 2) * (b_sub >> 4) + (kk & 3) * 2);
+}
+
 // ------------------------------------------------------------------ the GEMM kernel
 
 // EPI: the epilogue (fwd / dgrad: EPI_BF16; wgrad: any, EPI_PARTIAL for the split form).
@@ -541,11 +553,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- TMA producer (both CTAs)
         if (lane == 0) {
             const uint32_t full0 = mapa_shared(smem_u32(&c->full[0]), 0u);
-            // wgrad only: fwd / dgrad copies and stores take the default L2 policy (eviction
-            // hints measured no faster there).
-            const uint64_t pol_a = make_l2_policy(l2_field(p.l2, 0));
-            const uint64_t pol_b = make_l2_policy(l2_field(p.l2, 1));
-            const uint64_t pol_r = make_l2_policy(l2_field(p.l2, 3));
             int stage = 0, jt = 0;   // jt: units with a tail step so far
             uint32_t phase = 0;
             bool ok = true;
@@ -561,7 +568,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     p.prefetch && fa + kBM <= p.N)
                     // The epilogue reads this CTA's 128 x 256 block of out after the unit's
                     // mainloop: start bringing it into L2 now (whole 128-row blocks only).
-                    tma_prefetch_3d(&p.tmPre, t.c0, fa, t.e, pol_r);
+                    tma_prefetch_3d(&p.tmPre, t.c0, fa, t.e);
                 if (OP == OP_WGRAD) {
                     const int v = tail_rows(t.nred, t.nkb);
                     if (v) {
@@ -576,10 +583,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const int xb = (t.c0 + (kBN / 2) * static_cast<int>(pr.rank));
                         uint8_t* tbuf = tail_area + tb * kTailBytes;
                         mbar_arrive_expect_tx(&c->tb_full[tb], kTailBytes);
-                        tma_load_2d(tbuf, &p.tmTail[0], &c->tb_full[tb], fa, rt0, pol_a);
-                        tma_load_2d(tbuf + kTailSub, &p.tmTail[0], &c->tb_full[tb], fa + 64, rt0, pol_a);
-                        tma_load_2d(tbuf + 2 * kTailSub, &p.tmTail[1], &c->tb_full[tb], xb, rt0, pol_b);
-                        tma_load_2d(tbuf + 3 * kTailSub, &p.tmTail[1], &c->tb_full[tb], xb + 64, rt0, pol_b);
+                        tma_load_2d(tbuf, &p.tmTail[0], &c->tb_full[tb], fa, rt0);
+                        tma_load_2d(tbuf + kTailSub, &p.tmTail[0], &c->tb_full[tb], fa + 64, rt0);
+                        tma_load_2d(tbuf + 2 * kTailSub, &p.tmTail[1], &c->tb_full[tb], xb, rt0);
+                        tma_load_2d(tbuf + 3 * kTailSub, &p.tmTail[1], &c->tb_full[tb], xb + 64, rt0);
                         ++jt;
                     }
                 }
@@ -614,10 +621,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         // 128 reduction rows x this CTA's two 64-wide blocks of G and of X.
                         const int r = t.r0 + kb * kBK;
                         const int xb = t.c0 + (kBN / 2) * static_cast<int>(pr.rank);
-                        tma_load_2d_pair(a, &p.tmA, fb, fa, r, pol_a);
-                        tma_load_2d_pair(a + kSubBytes, &p.tmA, fb, fa + 64, r, pol_a);
-                        tma_load_2d_pair(b, &p.tmB[0], fb, xb, r, pol_b);
-                        tma_load_2d_pair(b + kSubBytes, &p.tmB[0], fb, xb + 64, r, pol_b);
+                        tma_load_2d_pair(a, &p.tmA, fb, fa, r);
+                        tma_load_2d_pair(a + kSubBytes, &p.tmA, fb, fa + 64, r);
+                        tma_load_2d_pair(b, &p.tmB[0], fb, xb, r);
+                        tma_load_2d_pair(b + kSubBytes, &p.tmB[0], fb, xb + 64, r);
                     }
                     if (++stage == R::kStages) { stage = 0; phase ^= 1u; }
                 }
@@ -654,9 +661,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (OP != OP_WGRAD) row_split(t.ncols, n_mma, half, bi);
                 const uint32_t idesc = idesc_bf16(kPairM, static_cast<uint32_t>(n_mma),
                                                   OP != OP_FWD, OP == OP_WGRAD);
-                // K-major sub-tiles: 16-element steps are 32 B apart within a 64-wide block,
-                // blocks are sub-tile bytes apart.  MN-major: 16 reduction rows are 2 KB apart;
-                // the two 64-wide M/N blocks are kSubBytes apart (LBO).
+                // MN-major operands: the two 64-wide M/N blocks are kSubBytes apart (LBO).
                 const uint32_t b_sub = static_cast<uint32_t>((8 << bi) * 128);
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(A * kBN);
                 const int tv = (OP == OP_WGRAD) ? tail_rows(t.nred, t.nkb) : 0;
@@ -678,17 +683,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const bool tstep = tv != 0 && kb == t.nkb - 1;
                         const int nsteps = tstep ? (valid >> 4)
                                                  : (valid < kBK ? (valid + 15) >> 4 : kBK / 16);
-                        for (int kk = 0; kk < nsteps; ++kk) {
-                            const uint32_t kblk = static_cast<uint32_t>(kk >> 2), k16 = kk & 3;
-                            const uint64_t ad =
-                                (OP == OP_FWD)
-                                    ? sdesc_sw128(a_addr + kblk * kSubBytes + k16 * 32, 16, 1024)
-                                    : sdesc_sw128(a_addr + kk * 2048, kSubBytes, 1024);
-                            const uint64_t bd =
-                                (OP == OP_WGRAD)
-                                    ? sdesc_sw128(b_addr + kk * 2048, kSubBytes, 1024)
-                                    : sdesc_sw128(b_addr + kblk * b_sub + k16 * 32, 16, 1024);
-                            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+                        // One base descriptor per operand and stage; step kk adds its byte offset
+                        // / 16 to the address field (bits 0-13), which never carries out of it
+                        // (shared memory is below 256 KB).  This thread issues every MMA of the
+                        // pair, so its work per MMA bounds the mainloop: full stages run an
+                        // unrolled loop of constant offsets.
+                        const uint64_t a0 = (OP == OP_FWD) ? sdesc_sw128(a_addr, 16, 1024)
+                                                           : sdesc_sw128(a_addr, kSubBytes, 1024);
+                        const uint64_t b0 = (OP == OP_WGRAD) ? sdesc_sw128(b_addr, kSubBytes, 1024)
+                                                             : sdesc_sw128(b_addr, 16, 1024);
+                        const uint32_t acc0 = kb != kb0 ? 1u : 0u;
+                        if (nsteps == kBK / 16) {
+#pragma unroll
+                            for (int kk = 0; kk < kBK / 16; ++kk)
+                                umma_bf16_pair(d_tmem, a0 + a_step<OP>(kk), b0 + b_step<OP>(kk, b_sub),
+                                               idesc, kk ? 1u : acc0);
+                        } else {
+                            for (int kk = 0; kk < nsteps; ++kk)
+                                umma_bf16_pair(d_tmem, a0 + a_step<OP>(kk), b0 + b_step<OP>(kk, b_sub),
+                                               idesc, kk ? 1u : acc0);
                         }
                         umma_commit_pair(&c->empty[stage], 3);
                         if (++stage == R::kStages) { stage = 0; phase ^= 1u; }
@@ -766,8 +779,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int rr = lane >> 2, gg = lane & 3;        // line-order phase: rows rr + 8j, chunk gg
         uint8_t* wslot = box + lane * 64;               // this lane's row in the write phase
         const int wsw = (lane >> 1) & 3;                // 64-byte swizzle: chunk g at g ^ wsw
-        const uint64_t pol_o = make_l2_policy(l2_field(p.l2, 2));
-        const uint64_t pol_r = make_l2_policy(l2_field(p.l2, 3));
         bool ok = true;
         int nextb = 0;
         Acq acq;                        // the MMA issuer's buffer plan, followed step by step
@@ -815,8 +826,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (b < nbox)
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
-                                old[b][j] = inside(b, j) ? ld_global_v4(gseg + b * 64 + 8 * j * ldo, pol_r)
-                                                         : make_uint4(0, 0, 0, 0);
+                                old[b][j] = inside(b, j) ? *reinterpret_cast<const uint4*>(
+                                                              gseg + b * 64 + 8 * j * ldo)
+                                                        : make_uint4(0, 0, 0, 0);
                 }
             };
             int fb = A;                 // the buffer that ends up holding the unit's value
@@ -922,14 +934,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             v.w = pack_bf16x2(__fadd_rn(bf16_lo(o.w), bf16_lo(v.w)), __fadd_rn(bf16_hi(o.w), bf16_hi(v.w)));
                         }
                     }
-                    if (inside(b, j)) st_global_v4(gline + 8 * j * ldo, v, pol_o);
+                    if (inside(b, j)) *reinterpret_cast<uint4*>(gline + 8 * j * ldo) = v;
                 }
                 if constexpr (acc) {
                     if (b + kAhead < nbox)
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             old[b % kAhead][j] = inside(b + kAhead, j)
-                                                     ? ld_global_v4(gseg + (b + kAhead) * 64 + 8 * j * ldo, pol_r)
+                                                     ? *reinterpret_cast<const uint4*>(
+                                                           gseg + (b + kAhead) * 64 + 8 * j * ldo)
                                                      : make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();   // the box is rewritten by the next box

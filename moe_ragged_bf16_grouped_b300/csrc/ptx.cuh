@@ -41,43 +41,13 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
 }
 
-// L2 eviction priority of a copy, load or store (createpolicy.fractional with fraction 1.0:
-// every line the access touches gets the priority).
-enum L2Pol : int { L2_NORMAL = 0, L2_EVICT_LAST = 1, L2_EVICT_FIRST = 2 };
-
-__device__ __forceinline__ uint64_t make_l2_policy(int kind) {
-    uint64_t pol;
-    if (kind == L2_EVICT_LAST)
-        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    else if (kind == L2_EVICT_FIRST)
-        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    else
-        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar,
-                                            int32_t x, int32_t y, uint64_t pol) {
+                                            int32_t x, int32_t y) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(m), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(pol)
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(m), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
-}
-
-// 16-byte global load / store with an L2 eviction policy.
-__device__ __forceinline__ uint4 ld_global_v4(const void* ptr, uint64_t pol) {
-    uint4 v;
-    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(ptr), "l"(pol));
-    return v;
-}
-
-__device__ __forceinline__ void st_global_v4(void* ptr, uint4 v, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr),
-                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
-                 : "memory");
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later
@@ -161,10 +131,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t m, uint32_t n, bool a
 // ---------------------------------------------------------------- TMA L2 prefetch
 // Brings a tile of the tensor into L2 (no shared memory involved).
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int32_t x, int32_t y,
-                                                int32_t z, uint64_t pol) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile.L2::cache_hint"
-                 " [%0, {%1, %2, %3}], %4;" ::"l"(m),
-                 "r"(x), "r"(y), "r"(z), "l"(pol)
+                                                int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(m),
+                 "r"(x), "r"(y), "r"(z)
                  : "memory");
 }
 
@@ -242,25 +211,6 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
         "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(m), "r"(mbar), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
-
-// The same copies with an L2 eviction policy (make_l2_policy).
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint32_t mbar,
-                                                 int32_t x, int32_t y, uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(m), "r"(mbar), "r"(x), "r"(y), "l"(pol)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m, uint32_t mbar,
-                                                 int32_t x, int32_t y, int32_t z, uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-        "l"(m), "r"(mbar), "r"(x), "r"(y), "r"(z), "l"(pol)
         : "memory");
 }
 
