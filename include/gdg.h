@@ -230,6 +230,34 @@ GDG_API gdg_status gdg_plan_launch(const gdg_plan* plan, void* stream);
 /* Frees a plan (NULL is ignored).  Must not race with a launch of the same plan. */
 GDG_API void gdg_plan_destroy(gdg_plan* plan);
 
+/*
+ * Non-deterministic weight gradient (the MoE grouped GEMM pull request's non-deterministic
+ * package, "Mode rules": its weight gradient may add the row chunks of its split form in an
+ * unordered way, every other path runs in a fixed order).  deterministic must be 0 (the
+ * caller states that it accepts results that vary from run to run); any other value returns
+ * GDG_EINVAL with nothing launched, and the deterministic entry is grouped_det_gemm_wgrad.
+ *
+ * Arguments, layouts, refusals and split_rows are those of grouped_det_gemm_wgrad.  When the
+ * split form is chosen (split_rows > 0, or 0 and the shapes pick it), every row chunk adds
+ * its fp32 tile into the result with unordered atomic fp32 adds instead of writing a partial
+ * for an ordered reduce: the summation order of the chunks, and so the low bits of dW, vary
+ * from run to run, and the adds flush subnormal values to zero.  An fp32 out receives the
+ * adds directly (zeroed first unless accumulate); a bf16 out needs an fp32 workspace of
+ * grouped_gemm_wgrad_workspace_bytes bytes that receives them, after which dW is rounded to
+ * bf16 (and added to out in bf16 with accumulate).  An empty group leaves out as it was
+ * (accumulate) or at +0.0.  The unsplit form (split_rows == -1, or 0 and the shapes pick it)
+ * is the deterministic kernel, bitwise equal to grouped_det_gemm_wgrad.
+ */
+GDG_API gdg_status grouped_gemm_wgrad(const gdg_args* args, const int32_t* offs, int E, int N,
+                                      int K, gdg_dtype out_dtype, int accumulate,
+                                      int deterministic, void* stream);
+
+/* Workspace bytes grouped_gemm_wgrad needs: E * N * K * 4 for a bf16 out in the split form,
+ * else 0.  (size_t)-1 for invalid arguments. */
+GDG_API size_t grouped_gemm_wgrad_workspace_bytes(int64_t rows, int E, int N, int K,
+                                                  gdg_dtype out_dtype, int accumulate,
+                                                  int32_t split_rows);
+
 /* Bytes of the library's own fixed scratch used by grouped_det_gemm_wgrad_noalloc. */
 #define GDG_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -29,6 +29,7 @@ __all__ = [
     "prepare_grouped_det_gemm_fwd", "prepare_grouped_det_gemm_dgrad",
     "prepare_grouped_det_gemm_wgrad", "grouped_det_mm", "GroupedDetMm",
     "gdg_status_string", "gdg_device_error", "gdg_device_error_async", "library_path",
+    "grouped_gemm_wgrad", "grouped_gemm_wgrad_workspace_bytes",
 ]
 
 GDG_OK, GDG_EINVAL, GDG_EALIGN, GDG_EOVERLAP, GDG_EWORKSPACE, GDG_ECUDA, GDG_ETIMEOUT = range(7)
@@ -57,6 +58,14 @@ for _name in ("grouped_det_gemm_fwd", "grouped_det_gemm_dgrad", "grouped_det_gem
     _f.restype = ctypes.c_int
     _f.argtypes = [ctypes.POINTER(GdgArgs), ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+_lib.grouped_gemm_wgrad.restype = ctypes.c_int
+_lib.grouped_gemm_wgrad.argtypes = [ctypes.POINTER(GdgArgs), ctypes.c_void_p, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_void_p]
+_lib.grouped_gemm_wgrad_workspace_bytes.restype = ctypes.c_size_t
+_lib.grouped_gemm_wgrad_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int32]
 _lib.grouped_det_gemm_workspace_bytes.restype = ctypes.c_size_t
 _lib.grouped_det_gemm_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -396,6 +405,79 @@ def grouped_det_gemm_wgrad_noalloc(g: torch.Tensor, x: torch.Tensor, offs: torch
                    *_out_strides(out))
     _call(_lib.grouped_det_gemm_wgrad_noalloc, "grouped_det_gemm_wgrad_noalloc", args, offs, E,
           N, K, _dtype_code(out.dtype), int(accumulate), _stream_ptr(stream, g.device))
+    return out
+
+
+def grouped_gemm_wgrad_workspace_bytes(rows: int, E: int, N: int, K: int,
+                                       out_dtype: torch.dtype = torch.bfloat16,
+                                       accumulate: bool = False, split_rows: int = 0) -> int:
+    n = _lib.grouped_gemm_wgrad_workspace_bytes(rows, E, N, K, _dtype_code(out_dtype),
+                                                int(accumulate), split_rows)
+    if n == ctypes.c_size_t(-1).value:
+        raise GdgError(GDG_EINVAL, "grouped_gemm_wgrad_workspace_bytes")
+    return n
+
+
+def grouped_gemm_wgrad(g: torch.Tensor, x: torch.Tensor, offs: torch.Tensor,
+                       out: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
+                       num_groups: int | None = None, *, deterministic=True,
+                       accumulate: bool = False, split_rows: int = 0,
+                       workspace: torch.Tensor | None = None, offs_kind=GDG_OFFS_ENDS,
+                       stream=None) -> torch.Tensor:
+    """Non-deterministic weight gradient (the MoE grouped GEMM pull request's non-deterministic
+    package, "Mode rules"): as grouped_det_gemm_wgrad, except that the row chunks of the split
+    form are added with unordered fp32 atomics, so dW varies in its low bits from run to run.
+
+    ``deterministic`` is keyword-only and only the bool False runs; any other value raises
+    ValueError naming the deterministic entry.  Under ``torch.use_deterministic_algorithms(True)``
+    a call that takes the split form raises RuntimeError before launching (``warn_only=True``:
+    one UserWarning, then the launch); the unsplit form runs in a fixed order and never alerts."""
+    if deterministic is not False:
+        raise ValueError("grouped_gemm_wgrad is the non-deterministic entry: pass "
+                         "deterministic=False for the non-deterministic path, or call "
+                         "grouped_det_gemm_wgrad for the deterministic one")
+    kind = _offs_kind(offs_kind)
+    _check_operand(g, "g", ndim=2)
+    _check_operand(x, "x", ndim=2)
+    rows, N = g.shape
+    if x.shape[0] != rows:
+        raise ValueError("g and x must have the same number of rows")
+    K = x.shape[1]
+    E = _num_groups(offs, kind)
+    if num_groups is not None and num_groups != E:
+        raise ValueError("num_groups does not match offs")
+    if out is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs out")
+        out = torch.empty((E, N, K), dtype=out_dtype or torch.bfloat16, device=g.device)
+    if out_dtype is not None and out_dtype != out.dtype:
+        raise ValueError("out_dtype must be None or out.dtype")
+    _check_out(out, out.dtype, 3)
+    if tuple(out.shape) != (E, N, K):
+        raise ValueError("out must be [E, N, K]")
+    _same_device(offs, g, x, out, workspace)
+    resolved = split_rows if split_rows != 0 else grouped_det_gemm_auto_split_rows(rows, E, N, K)
+    if resolved > 0 and rows > 0 and torch.are_deterministic_algorithms_enabled():
+        msg = ("grouped_gemm_wgrad adds the row chunks of its split form in an unordered way; "
+               "grouped_det_gemm_wgrad is the deterministic entry")
+        if torch.is_deterministic_algorithms_warn_only_enabled():
+            import warnings
+            warnings.warn(msg, UserWarning, stacklevel=2)
+        else:
+            raise RuntimeError(msg)
+    need = grouped_gemm_wgrad_workspace_bytes(rows, E, N, K, out.dtype, accumulate, split_rows)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=g.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    args = GdgArgs(g.data_ptr(), x.data_ptr(), out.data_ptr(), ws_ptr, ws_bytes, rows, kind,
+                   split_rows, *_out_strides(out))
+    with torch.cuda.device(offs.device):
+        st = _lib.grouped_gemm_wgrad(ctypes.byref(args), offs.data_ptr(), E, N, K,
+                                     _dtype_code(out.dtype), int(accumulate), 0,
+                                     _stream_ptr(stream, g.device))
+    if st != GDG_OK:
+        raise GdgError(st, "grouped_gemm_wgrad")
     return out
 
 

@@ -18,6 +18,7 @@
 namespace {
 
 using gdg::GemmParams;
+using gdg::DenseParams;
 using gdg::ReduceParams;
 
 __device__ unsigned int g_device_error = 0;
@@ -167,7 +168,8 @@ DeviceInfo* device_info(gdg_status* st) {
             set_up_kernel<gdg::OP_WGRAD, gdg::EPI_FP32, 256>(d.sms, &d.pairs) != cudaSuccess ||
             set_up_kernel<gdg::OP_WGRAD, gdg::EPI_BF16_ACC, 256>(d.sms, &d.pairs) != cudaSuccess ||
             set_up_kernel<gdg::OP_WGRAD, gdg::EPI_FP32_ACC, 256>(d.sms, &d.pairs) != cudaSuccess ||
-            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_PARTIAL, 256>(d.sms, &d.pairs) != cudaSuccess) {
+            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_PARTIAL, 256>(d.sms, &d.pairs) != cudaSuccess ||
+            set_up_kernel<gdg::OP_WGRAD, gdg::EPI_RED, 256>(d.sms, &d.pairs) != cudaSuccess) {
             *st = GDG_ECUDA;
             return nullptr;
         }
@@ -296,10 +298,14 @@ struct Plan {
     int epi = 0;             // wgrad kernel's epilogue (EPI_PARTIAL for the split form)
     bool launch = false;     // false: the call has nothing to launch (rows == 0 cases)
     bool reduce = false;     // split form: ordered reduce of the partials after the GEMM
+    bool zero = false;       // unordered split form: zero the fp32 destination first
+    bool finish = false;     // unordered split form, bf16 out: round the fp32 sums into out
     int grid = 0;
     int rgrid = 0;
     GemmParams p;
     ReduceParams r;
+    DenseParams z;           // zero kernel
+    DenseParams f;           // finish kernel
 };
 
 // fwd (OP_FWD) and dgrad (OP_DGRAD) share everything but the operand maps.
@@ -359,8 +365,11 @@ gdg_status plan_fwd_like(const gdg_args* args, const int32_t* offs, int E, int N
     return GDG_OK;
 }
 
+// wgrad plan.  ordered = 0 selects the non-deterministic form: row chunks of the split form
+// add their fp32 tiles into the destination with unordered atomic adds (no partials, no
+// ordered reduce); the unsplit form runs in its fixed order either way.
 gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, int K,
-                      gdg_dtype out_dtype, int accumulate, Plan* pl) {
+                      gdg_dtype out_dtype, int accumulate, Plan* pl, int ordered = 1) {
     gdg_status st = check_common(args, offs, E, N, K, out_dtype);
     if (st != GDG_OK) return st;
     if (accumulate != 0 && accumulate != 1) return GDG_EINVAL;
@@ -392,10 +401,12 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
     int64_t max_units = static_cast<int64_t>(E) * tiles_per_expert(N, K);
     if (split) {
         max_units = split_max_units(rows, E, N, K, split_rows);
-        const size_t need = static_cast<size_t>(max_units) * gdg::kPartialElems * sizeof(float);
-        if (!args->workspace || args->workspace_bytes < need) return GDG_EWORKSPACE;
-        if (!aligned16(args->workspace)) return GDG_EALIGN;
-        const Range r_w = range_of(args->workspace, need);
+        // ordered: the fp32 partial tiles; unordered: the fp32 sums of a bf16 out (none for fp32)
+        const size_t need = ordered ? static_cast<size_t>(max_units) * gdg::kPartialElems * sizeof(float)
+                                    : (out_dtype == GDG_FP32 ? 0 : static_cast<size_t>(E) * N * K * 4);
+        if (need > 0 && (!args->workspace || args->workspace_bytes < need)) return GDG_EWORKSPACE;
+        if (need > 0 && !aligned16(args->workspace)) return GDG_EALIGN;
+        const Range r_w = range_of(need > 0 ? args->workspace : nullptr, need);
         if (overlaps(r_w, r_out) || overlaps(r_w, r_o) ||
             (rows > 0 && (overlaps(r_w, r_a) || overlaps(r_w, r_b))))
             return GDG_EOVERLAP;
@@ -440,8 +451,40 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
     pl->grid = pair_grid(max_units, dev->pairs);
     pl->epi = split ? static_cast<int>(gdg::EPI_PARTIAL) : epi;
     pl->launch = true;
-    pl->reduce = split;
-    if (split) {
+    pl->reduce = split && ordered;
+    const int64_t vec4 = static_cast<int64_t>(E) * N * K / 4;
+    int64_t dgrid = ceil_div(vec4, gdg::kReduceThreads);
+    if (dgrid > static_cast<int64_t>(dev->sms) * 8) dgrid = static_cast<int64_t>(dev->sms) * 8;
+    if (split && !ordered) {
+        // The unordered adds go into out itself (fp32) or into the fp32 workspace (bf16), which
+        // starts at +0.0 unless an fp32 out is accumulated into.
+        const bool f32 = out_dtype == GDG_FP32;
+        pl->epi = gdg::EPI_RED;
+        p.partial = nullptr;
+        if (!f32) {
+            p.out = args->workspace;
+            p.ld_out = K;
+            p.es_out = static_cast<int64_t>(N) * K;
+        }
+        pl->zero = !f32 || !accumulate;
+        pl->z.out = p.out;
+        pl->z.E = E;
+        pl->z.N = N;
+        pl->z.K = K;
+        pl->z.ld_out = p.ld_out;
+        pl->z.es_out = p.es_out;
+        pl->finish = !f32;
+        pl->f.out = args->out;
+        pl->f.acc = static_cast<const float*>(args->workspace);
+        pl->f.E = E;
+        pl->f.N = N;
+        pl->f.K = K;
+        pl->f.epi = accumulate ? gdg::EPI_BF16_ACC : gdg::EPI_BF16;
+        pl->f.ld_out = L.ld;
+        pl->f.es_out = L.es;
+        pl->rgrid = static_cast<int>(dgrid);
+    }
+    if (split && ordered) {
         ReduceParams& r = pl->r;
         r.offs = offs;
         r.partial = static_cast<const float*>(args->workspace);
@@ -456,10 +499,7 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
         r.max_units = static_cast<int>(max_units);
         r.ld_out = L.ld;
         r.es_out = L.es;
-        const int64_t vec4 = static_cast<int64_t>(E) * N * K / 4;
-        int64_t rgrid = ceil_div(vec4, gdg::kReduceThreads);
-        if (rgrid > static_cast<int64_t>(dev->sms) * 8) rgrid = static_cast<int64_t>(dev->sms) * 8;
-        pl->rgrid = static_cast<int>(rgrid);
+        pl->rgrid = static_cast<int>(dgrid);
     }
     return GDG_OK;
 }
@@ -471,6 +511,11 @@ gdg_status launch_plan(const Plan& pl, cudaStream_t s) {
     cudaGetLastError();
     const GemmParams& p = pl.p;
     const int g = pl.grid;
+    if (pl.zero) {
+        gdg::zero_f32_kernel<<<pl.rgrid, gdg::kReduceThreads, 0, s>>>(pl.z);
+        const gdg_status st = launch_status(cudaGetLastError());
+        if (st != GDG_OK) return st;
+    }
     if (pl.op == GDG_OP_FWD) {
         if (pl.rt == 128)
             gdg::grouped_gemm_kernel<gdg::OP_FWD, gdg::EPI_BF16, 128><<<g, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
@@ -498,12 +543,20 @@ gdg_status launch_plan(const Plan& pl, cudaStream_t s) {
         case gdg::EPI_FP32_ACC:
             gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_FP32_ACC, 256><<<g, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
             break;
+        case gdg::EPI_RED:
+            gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_RED, 256><<<g, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
+            break;
         default:
             gdg::grouped_gemm_kernel<gdg::OP_WGRAD, gdg::EPI_PARTIAL, 256><<<g, gdg::kThreads, gdg::kGemmSmemBytes, s>>>(p);
             break;
     }
     gdg_status st = launch_status(cudaGetLastError());
-    if (st != GDG_OK || !pl.reduce) return st;
+    if (st != GDG_OK) return st;
+    if (pl.finish) {
+        gdg::finish_bf16_kernel<<<pl.rgrid, gdg::kReduceThreads, 0, s>>>(pl.f);
+        return launch_status(cudaGetLastError());
+    }
+    if (!pl.reduce) return st;
     gdg::wgrad_reduce_kernel<<<pl.rgrid, gdg::kReduceThreads, 0, s>>>(pl.r);
     return launch_status(cudaGetLastError());
 }
@@ -562,6 +615,27 @@ size_t grouped_det_gemm_workspace_bytes(int op, int64_t rows, int E, int N, int 
 gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* offs, int E, int N,
                                   int K, gdg_dtype out_dtype, int accumulate, void* stream) {
     return run(GDG_OP_WGRAD, args, offs, E, N, K, out_dtype, accumulate, stream);
+}
+
+gdg_status grouped_gemm_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, int K,
+                              gdg_dtype out_dtype, int accumulate, int deterministic, void* stream) {
+    if (deterministic != 0) return GDG_EINVAL;
+    Plan pl;
+    const gdg_status st = plan_wgrad(args, offs, E, N, K, out_dtype, accumulate, &pl, 0);
+    if (st != GDG_OK) return st;
+    return launch_plan(pl, static_cast<cudaStream_t>(stream));
+}
+
+size_t grouped_gemm_wgrad_workspace_bytes(int64_t rows, int E, int N, int K, gdg_dtype out_dtype,
+                                          int accumulate, int32_t split_rows) {
+    if (E < 1 || E > GDG_MAX_EXPERTS || N <= 0 || K <= 0 || rows < 0 || N % 8 || K % 8 ||
+        (out_dtype != GDG_BF16 && out_dtype != GDG_FP32))
+        return static_cast<size_t>(-1);
+    (void)accumulate;
+    if (split_rows == 0) split_rows = auto_split_rows(rows, E, N, K);
+    if (split_rows < 0 || rows == 0 || out_dtype == GDG_FP32) return 0;
+    if (split_rows % 64 != 0) return static_cast<size_t>(-1);
+    return static_cast<size_t>(E) * N * K * 4;
 }
 
 struct gdg_plan {

@@ -86,7 +86,10 @@ constexpr uint32_t kSuspendNs = 20000;             // sleep hint of a waiting th
 constexpr uint64_t kCopyDrainNs = 2000000ull;   // after an abort: copies in flight land by then
 
 enum Op : int { OP_FWD = 0, OP_DGRAD = 1, OP_WGRAD = 2 };
-enum Epi : int { EPI_BF16 = 0, EPI_FP32 = 1, EPI_BF16_ACC = 2, EPI_FP32_ACC = 3, EPI_PARTIAL = 4 };
+// EPI_RED (non-deterministic split form): each row chunk's fp32 tile is added into an fp32
+// destination with unordered atomic adds instead of being stored as a partial.
+enum Epi : int { EPI_BF16 = 0, EPI_FP32 = 1, EPI_BF16_ACC = 2, EPI_FP32_ACC = 3, EPI_PARTIAL = 4,
+                 EPI_RED = 5 };
 
 constexpr unsigned kDevErrTimeout = 6u;
 
@@ -137,9 +140,33 @@ constexpr size_t kGemmSmemBytes =
 
 // ------------------------------------------------------------------ schedule
 
+// Division of 0 <= n < 2^31 by a divisor d >= 1 fixed for the launch, by multiplication
+// (Granlund and Montgomery, "Division by invariant integers using multiplication", 1994):
+// with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1, n / d = (umulhi(n, m) + n) >> l
+// (the sum stays below 2^32 because umulhi(n, m) < n < 2^31).
+struct FastDiv {
+    uint32_t d, m, l;
+    __host__ __device__ static FastDiv make(uint32_t d) {
+        FastDiv f;
+        f.d = d;
+        f.l = 0;
+        while ((1ull << f.l) < d) ++f.l;
+        f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << f.l) - d)) / d + 1);
+        return f;
+    }
+    __host__ __device__ uint32_t div(uint32_t n) const {
+#ifdef __CUDA_ARCH__
+        return (__umulhi(n, m) + n) >> l;
+#else
+        return static_cast<uint32_t>(((static_cast<uint64_t>(n) * m >> 32) + n) >> l);
+#endif
+    }
+};
+
 struct Shape {
     int ft;     // feature tiles (fwd, dgrad) or tiles per expert (wgrad), 256 wide
     int kt;     // wgrad: k tiles per expert
+    FastDiv ft_div, kt_div;   // wgrad: division by ft and by kt in the unit decode
 };
 
 template <int OP>
@@ -148,20 +175,34 @@ __device__ __forceinline__ Shape unit_shape(const GemmParams& p) {
     if (OP == OP_FWD) { s.ft = (p.N + kPairM - 1) / kPairM; s.kt = 1; }
     else if (OP == OP_DGRAD) { s.ft = (p.K + kPairM - 1) / kPairM; s.kt = 1; }
     else { s.kt = (p.K + kBN - 1) / kBN; s.ft = ((p.N + kPairM - 1) / kPairM) * s.kt; }
+    s.ft_div = FastDiv::make(static_cast<uint32_t>(s.ft));
+    s.kt_div = FastDiv::make(static_cast<uint32_t>(s.kt));
     return s;
 }
 
-// Rows [s, s + m) of group e, clamped to [0, rows]; a reversed range is empty.
-__device__ __forceinline__ void group_range(const int32_t* offs, int kind, int64_t rows, int e,
-                                            int& s, int& m) {
-    int64_t a, b;
+// The offsets that bound group e: its first row a and its end b, as stored.
+__device__ __forceinline__ void group_raw(const int32_t* offs, int kind, int e, int32_t& a,
+                                          int32_t& b) {
     if (kind == 0) { a = e > 0 ? __ldg(offs + e - 1) : 0; b = __ldg(offs + e); }
     else { a = __ldg(offs + e); b = __ldg(offs + e + 1); }
+}
+
+// Rows [s, s + m) of a group bounded by a and b, clamped to [0, rows]; a reversed range is
+// empty.
+__device__ __forceinline__ void group_clamp(int64_t a, int64_t b, int64_t rows, int& s, int& m) {
     a = a < 0 ? 0 : (a > rows ? rows : a);
     b = b < 0 ? 0 : (b > rows ? rows : b);
     if (b < a) b = a;
     s = static_cast<int>(a);
     m = static_cast<int>(b - a);
+}
+
+// Rows [s, s + m) of group e.
+__device__ __forceinline__ void group_range(const int32_t* offs, int kind, int64_t rows, int e,
+                                            int& s, int& m) {
+    int32_t a, b;
+    group_raw(offs, kind, e, a, b);
+    group_clamp(a, b, rows, s, m);
 }
 
 // Units of a group of m rows.  64-bit: with offsets that are not cumulative (several groups
@@ -262,6 +303,7 @@ __device__ int count_units(const GemmParams& p, const Shape& sh, int64_t* warp_t
 struct Cursor {
     int64_t base, n;
     int pos, e, s, m;
+    int32_t na, nb, na2, nb2;   // the offsets of the walk's next two groups, loaded ahead
     const uint16_t* order;      // nullptr: natural order
 };
 
@@ -283,6 +325,17 @@ __device__ __forceinline__ void sort_groups_by_size(const GemmParams& p, uint16_
     }
 }
 
+// Issues the loads of the offsets of the walk's group pos + d (if any); their values are first
+// used when the cursor reaches that group, so the load latency is hidden (two groups ahead: one
+// unit step may cross two short groups).
+__device__ __forceinline__ void cursor_load(Cursor& cu, const GemmParams& p, int d, int32_t& a,
+                                            int32_t& b) {
+    if (cu.pos + d < p.E) {
+        const int e = cu.order ? cu.order[cu.pos + d] : cu.pos + d;
+        group_raw(p.offs, p.offs_kind, e, a, b);
+    }
+}
+
 template <int OP, int RT>
 __device__ __forceinline__ void cursor_init(Cursor& cu, const GemmParams& p, const Shape& sh,
                                             const uint16_t* order) {
@@ -292,6 +345,8 @@ __device__ __forceinline__ void cursor_init(Cursor& cu, const GemmParams& p, con
     cu.base = 0;
     group_range(p.offs, p.offs_kind, p.rows, cu.e, cu.s, cu.m);
     cu.n = units_of_group<OP, RT>(cu.m, sh, p.split_rows);
+    cursor_load(cu, p, 1, cu.na, cu.nb);
+    cursor_load(cu, p, 2, cu.na2, cu.nb2);
 }
 
 // Moves the cursor to the group that holds unit u (u never decreases between calls, and
@@ -303,8 +358,11 @@ __device__ __forceinline__ void cursor_seek(Cursor& cu, const GemmParams& p, con
         cu.base += cu.n;
         ++cu.pos;
         cu.e = cu.order ? cu.order[cu.pos] : cu.pos;
-        group_range(p.offs, p.offs_kind, p.rows, cu.e, cu.s, cu.m);
+        group_clamp(cu.na, cu.nb, p.rows, cu.s, cu.m);
         cu.n = units_of_group<OP, RT>(cu.m, sh, p.split_rows);
+        cu.na = cu.na2;
+        cu.nb = cu.nb2;
+        cursor_load(cu, p, 2, cu.na2, cu.nb2);
     }
 }
 
@@ -328,7 +386,8 @@ struct Acq {
 template <int OP, int EPI>
 __device__ __forceinline__ int chunks_of(int nkb) {
     constexpr bool chunked =
-        OP == OP_WGRAD && (EPI == EPI_FP32 || EPI == EPI_FP32_ACC || EPI == EPI_PARTIAL);
+        OP == OP_WGRAD &&
+        (EPI == EPI_FP32 || EPI == EPI_FP32_ACC || EPI == EPI_PARTIAL || EPI == EPI_RED);
     if (!chunked || nkb <= kChunkStages) return 1;
     return (nkb + kChunkStages - 1) / kChunkStages;
 }
@@ -366,9 +425,10 @@ __device__ __forceinline__ Tile decode_unit(const GemmParams& p, Cursor& cu, con
     const int local = static_cast<int>(u - cu.base);   // < cu.n, which fits an int
     const int s = cu.s, m = cu.m;
     if (OP == OP_WGRAD) {
-        const int sp = local / sh.ft;
+        const int sp = static_cast<int>(sh.ft_div.div(static_cast<uint32_t>(local)));
         const int rem = local - sp * sh.ft;
-        const int nt = rem / sh.kt, kt = rem - nt * sh.kt;
+        const int nt = static_cast<int>(sh.kt_div.div(static_cast<uint32_t>(rem)));
+        const int kt = rem - nt * sh.kt;
         t.f0 = nt * kPairM;
         t.c0 = kt * kBN;
         t.ncols = min(kBN, p.K - t.c0);
@@ -774,7 +834,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t tempty0 = mapa_shared(smem_u32(&c->tempty[0]), 0u);
         uint8_t* box = stage_area + ew * kEpiBoxBytes;
         constexpr bool acc = EPI == EPI_FP32_ACC || EPI == EPI_BF16_ACC;
-        constexpr bool f32 = EPI == EPI_FP32 || EPI == EPI_FP32_ACC || EPI == EPI_PARTIAL;
+        constexpr bool f32 =
+            EPI == EPI_FP32 || EPI == EPI_FP32_ACC || EPI == EPI_PARTIAL || EPI == EPI_RED;
         constexpr int osz = f32 ? 4 : 2;
         const int rr = lane >> 2, gg = lane & 3;        // line-order phase: rows rr + 8j, chunk gg
         uint8_t* wslot = box + lane * 64;               // this lane's row in the write phase
@@ -934,7 +995,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             v.w = pack_bf16x2(__fadd_rn(bf16_lo(o.w), bf16_lo(v.w)), __fadd_rn(bf16_hi(o.w), bf16_hi(v.w)));
                         }
                     }
-                    if (inside(b, j)) *reinterpret_cast<uint4*>(gline + 8 * j * ldo) = v;
+                    if (inside(b, j)) {
+                        if constexpr (EPI == EPI_RED) red_add_v4_f32(gline + 8 * j * ldo, v);
+                        else *reinterpret_cast<uint4*>(gline + 8 * j * ldo) = v;
+                    }
                 }
                 if constexpr (acc) {
                     if (b + kAhead < nbox)
@@ -1093,6 +1157,61 @@ __global__ void __launch_bounds__(kReduceThreads) wgrad_reduce_kernel(const __gr
             }
             *o = d;
         }
+    }
+}
+
+// ------------------------------------------------------------------ non-deterministic split
+
+struct DenseParams {
+    void* out;              // [E][N][K] with strides ld_out, es_out (elements)
+    const float* acc;       // finish: dense fp32 [E][N][K] sums
+    int E, N, K;
+    int epi;                // finish: EPI_BF16 or EPI_BF16_ACC
+    int64_t ld_out, es_out;
+};
+
+// out[e][n][k] = +0.0f over a strided fp32 [E][N][K] (the destination of the unordered adds).
+__global__ void __launch_bounds__(kReduceThreads) zero_f32_kernel(const __grid_constant__ DenseParams p) {
+    const int64_t NK = static_cast<int64_t>(p.N) * p.K;
+    const int64_t total4 = static_cast<int64_t>(p.E) * NK / 4;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kReduceThreads + threadIdx.x; i < total4;
+         i += static_cast<int64_t>(gridDim.x) * kReduceThreads) {
+        const int64_t idx = i * 4;
+        const int e = static_cast<int>(idx / NK);
+        const int64_t rem = idx - e * NK;
+        const int n = static_cast<int>(rem / p.K);
+        const int k = static_cast<int>(rem - static_cast<int64_t>(n) * p.K);
+        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + e * p.es_out +
+                                   static_cast<int64_t>(n) * p.ld_out + k) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// bf16 out from the fp32 sums: out = bf16(acc), or bf16(float(out) + float(bf16(acc))).
+__global__ void __launch_bounds__(kReduceThreads) finish_bf16_kernel(const __grid_constant__ DenseParams p) {
+    const int64_t NK = static_cast<int64_t>(p.N) * p.K;
+    const int64_t total4 = static_cast<int64_t>(p.E) * NK / 4;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kReduceThreads + threadIdx.x; i < total4;
+         i += static_cast<int64_t>(gridDim.x) * kReduceThreads) {
+        const int64_t idx = i * 4;
+        const int e = static_cast<int>(idx / NK);
+        const int64_t rem = idx - e * NK;
+        const int n = static_cast<int>(rem / p.K);
+        const int k = static_cast<int>(rem - static_cast<int64_t>(n) * p.K);
+        const float4 a = *reinterpret_cast<const float4*>(p.acc + idx);
+        uint2* o = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + e * p.es_out +
+                                            static_cast<int64_t>(n) * p.ld_out + k);
+        uint2 d;
+        d.x = pack_bf16x2(a.x, a.y);
+        d.y = pack_bf16x2(a.z, a.w);
+        if (p.epi == EPI_BF16_ACC) {
+            const uint2 old = *o;
+            d.x = pack_bf16x2(__fadd_rn(bf16_lo(old.x), bf16_lo(d.x)),
+                              __fadd_rn(bf16_hi(old.x), bf16_hi(d.x)));
+            d.y = pack_bf16x2(__fadd_rn(bf16_lo(old.y), bf16_lo(d.y)),
+                              __fadd_rn(bf16_hi(old.y), bf16_hi(d.y)));
+        }
+        *o = d;
     }
 }
 

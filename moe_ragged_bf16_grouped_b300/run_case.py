@@ -39,10 +39,18 @@ def main():
     ap.add_argument("--split-rows", type=int, default=0)
     ap.add_argument("--out-dtype", default=None, choices=(None, "bf16", "fp32"))
     ap.add_argument("--accumulate", action="store_true")
+    ap.add_argument("--nondet", action="store_true",
+                    help="wgrad: the non-deterministic entry (unordered adds of the split form)")
+    ap.add_argument("--shape", default=None,
+                    help="E,N,K,rows: equal groups of a synthetic shape instead of a workload")
     args = ap.parse_args()
 
     w = wl.WORKLOADS[args.workload]
     sizes = wl.SIZES[w.name](0)
+    if args.shape:
+        E, N, K, rows = (int(v) for v in args.shape.split(","))
+        sizes = np.full(E, rows // E, dtype=np.int64)
+        w = wl.Workload(f"shape_{E}x{N}x{K}x{rows}", E=E, N=N, K=K, ops=(), main_grad_std=0.01)
     if args.experts:
         sizes = sizes[:args.experts]
         w = wl.Workload(w.name, E=len(sizes), N=w.N, K=w.K, ops=w.ops,
@@ -64,12 +72,20 @@ def main():
     else:
         out = torch.zeros((w.E, w.N, w.K), dtype=torch.float32 if fp32 else torch.bfloat16,
                           device=dev)
-        need = gdg.grouped_det_gemm_workspace_bytes(gdg.GDG_OP_WGRAD, rows, w.E, w.N, w.K,
-                                                    out.dtype, acc, args.split_rows)
-        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
-        fn = lambda: gdg.grouped_det_gemm_wgrad(d["G"], d["X"], d["offs"], out=out,  # noqa: E731
+        if args.nondet:
+            need = gdg.grouped_gemm_wgrad_workspace_bytes(rows, w.E, w.N, w.K, out.dtype, acc,
+                                                          args.split_rows)
+            ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            fn = lambda: gdg.grouped_gemm_wgrad(d["G"], d["X"], d["offs"], out=out,  # noqa: E731
                                                 accumulate=acc, split_rows=args.split_rows,
-                                                workspace=ws)
+                                                workspace=ws, deterministic=False)
+        else:
+            need = gdg.grouped_det_gemm_workspace_bytes(gdg.GDG_OP_WGRAD, rows, w.E, w.N, w.K,
+                                                        out.dtype, acc, args.split_rows)
+            ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            fn = lambda: gdg.grouped_det_gemm_wgrad(d["G"], d["X"], d["offs"], out=out,  # noqa: E731
+                                                    accumulate=acc, split_rows=args.split_rows,
+                                                    workspace=ws)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
         fn()
@@ -89,7 +105,8 @@ def main():
     line = {"workload": w.name, "op": args.op, "E": w.E, "N": w.N, "K": w.K,
             "rows": M, "ms_median": med, "ms_min": float(np.min(ts)) if ts else None,
             "tflops": flops / med / 1e9 if ts else None,
-            "out_dtype": str(out.dtype), "accumulate": acc}
+            "out_dtype": str(out.dtype), "accumulate": acc, "split_rows": args.split_rows,
+            "nondet": bool(args.nondet)}
     e_ne = int(np.count_nonzero(sizes))
     if args.op == "wgrad":
         s_out = out.element_size()
