@@ -66,19 +66,6 @@ bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                       dims, strides_bytes, box);
 }
 
-// wgrad accumulate: out [E, N, K] (bf16 or fp32, row stride ld, expert stride es, in
-// elements) for L2 prefetches of 128 x 256 blocks of one expert.
-bool encode_prefetch(CUtensorMap* m, void* base, int E, int N, int K, int64_t ld, int64_t es,
-                     bool fp32) {
-    const uint64_t esz = fp32 ? 4u : 2u;
-    const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N),
-                              static_cast<uint64_t>(E)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(ld) * esz, static_cast<uint64_t>(es) * esz};
-    const uint32_t box[3] = {256u, 128u, 1u};
-    return encode_map(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      CU_TENSOR_MAP_SWIZZLE_NONE, base, 3, dims, strides, box);
-}
-
 // [rows, cols] bf16 as a plain 2-D map with box {64, box_rows}: one copy brings one 64-column
 // block of box_rows rows (box_rows x 128 B); columns and rows past the extent read as zeros.
 bool encode_rows_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, uint32_t box_rows) {
@@ -241,6 +228,15 @@ int pair_grid(int64_t units, int pairs) {
     if (cap > 0 && pairs > cap) pairs = cap;
     const int64_t n = units < pairs ? units : pairs;
     return static_cast<int>(2 * (n > 0 ? n : 1));
+}
+
+// wgrad, groups walked by size: the team schedule (grouped_gemm.cuh, assign_teams) when a
+// group's tiles are fewer than the launch's pairs and at most kMaxTeams teams result.
+int teams_rule(int sorted, int tiles_per_expert, int pairs) {
+    if (!sorted || tiles_per_expert >= pairs) return 0;
+    const int full = pairs / tiles_per_expert;
+    const int nteams = full + (pairs % tiles_per_expert ? 1 : 0);
+    return nteams <= gdg::kMaxTeams ? 1 : 0;
 }
 
 // wgrad, unsplit: walk the groups by decreasing size when groups are long on average (at least
@@ -429,11 +425,6 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
         !encode_rows_2d(&p.tmTail[0], a, map_rows, N, 16u) ||
         !encode_rows_2d(&p.tmTail[1], b, map_rows, K, 16u))
         return GDG_ECUDA;
-    // The prefetch map takes the common layouts (experts in address order, rows in order).
-    p.prefetch = !split && accumulate && L.es >= static_cast<int64_t>(N) * L.ld;
-    if (p.prefetch &&
-        !encode_prefetch(&p.tmPre, args->out, E, N, K, L.ld, L.es, out_dtype == GDG_FP32))
-        return GDG_ECUDA;
     p.offs = offs;
     p.out = args->out;
     p.partial = split ? static_cast<float*>(args->workspace) : nullptr;
@@ -449,6 +440,7 @@ gdg_status plan_wgrad(const gdg_args* args, const int32_t* offs, int E, int N, i
     p.es_out = L.es;
     p.sort_groups = split ? 0 : sort_groups_rule(rows, E);
     pl->grid = pair_grid(max_units, dev->pairs);
+    p.teams = teams_rule(p.sort_groups, tiles_per_expert(N, K), pl->grid / 2);
     pl->epi = split ? static_cast<int>(gdg::EPI_PARTIAL) : epi;
     pl->launch = true;
     pl->reduce = split && ordered;

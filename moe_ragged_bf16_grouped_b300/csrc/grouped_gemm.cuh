@@ -77,7 +77,8 @@ constexpr int kTailBufs = 2;
 constexpr int kThreads = 384;               // GEMM kernel: 4 role warps + 8 epilogue warps
 constexpr int kReduceThreads = 256;
 constexpr int kMaxE = 1024;
-constexpr int kMaxSorted = 256;             // wgrad: groups walked by size need E <= this
+constexpr int kMaxSorted = 128;             // wgrad: groups walked by size need E <= this
+constexpr int kMaxTeams = 32;               // wgrad teams (one warp computes the assignment)
 constexpr int kTmemCols = 512;
 constexpr int kPartialElems = kPairM * kBN; // fp32 elements per split partial tile
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // any single wait > 2 s is a hang
@@ -100,8 +101,6 @@ struct GemmParams {
                             // wgrad: G {N, rows} box {64, 128}
     CUtensorMap tmB[5];     // fwd: X {K, rows}, dgrad: G {N, rows}, box {64, 8 << i};
                             // wgrad: tmB[0] = X {K, rows} box {64, 128}
-    CUtensorMap tmPre;      // wgrad accumulate: out as {K, N, E} (its strides), box {256, 128, 1}
-                            // (L2 prefetch; only when prefetch != 0)
     CUtensorMap tmTail[2];  // wgrad tail steps: G {N, rows}, X {K, rows}, box {64, 16}
     const int32_t* offs;
     void* out;
@@ -113,10 +112,10 @@ struct GemmParams {
     int split_rows;         // wgrad: > 0 selects the split form
     int max_units;          // units at or past this index are skipped
     int test_withhold;      // test only: pair 0's even CTA arms its first stage but copies nothing
-    int prefetch;           // wgrad accumulate: tmPre is valid
     int64_t ld_out;         // out row stride (elements)
     int64_t es_out;         // wgrad: out expert stride (elements)
     int sort_groups;        // wgrad, unsplit, E <= kMaxSorted: walk the groups by size
+    int teams;              // sort_groups and tiles per expert < pairs: team schedule (below)
 };
 
 
@@ -133,6 +132,8 @@ struct SmemCtl {
     int abort_flag;
     int64_t warp_tot[kThreads / 32];
     uint16_t order[kMaxSorted];  // sort_groups: the groups by decreasing size (ties: index)
+    int32_t msize[kMaxSorted];   // sort_groups: the row count of order[i]
+    uint8_t team_of[kMaxSorted]; // teams: the team that runs order[i]
 };
 
 constexpr size_t kGemmSmemBytes =
@@ -311,7 +312,8 @@ struct Cursor {
 // and groups of similar length next to each other keep the pairs that share a group's rows
 // (every tile of it) working on them at the same time, so the rows are read from HBM once.
 // Every thread of the block calls it; a later __syncthreads publishes order[].
-__device__ __forceinline__ void sort_groups_by_size(const GemmParams& p, uint16_t* order) {
+__device__ __forceinline__ void sort_groups_by_size(const GemmParams& p, uint16_t* order,
+                                                   int32_t* msize) {
     for (int e = threadIdx.x; e < p.E; e += kThreads) {
         int s, m;
         group_range(p.offs, p.offs_kind, p.rows, e, s, m);
@@ -322,6 +324,38 @@ __device__ __forceinline__ void sort_groups_by_size(const GemmParams& p, uint16_
             rank += (mj > m || (mj == m && j < e)) ? 1 : 0;
         }
         order[rank] = static_cast<uint16_t>(e);
+        msize[rank] = m;
+    }
+}
+
+// Team schedule (wgrad, groups walked by size, T = tiles per expert below the pair count P):
+// the pairs form floor(P / T) full teams of T pairs, which run each of their groups as one
+// round (pair i of the team takes tile i), and, if P is not a multiple of T, a remainder team
+// of b = P mod T pairs, which runs each of its groups in ceil(T / b) rounds.  Every tile of a
+// group is then in flight at the same time (full team) or within one round (remainder team),
+// so the group's rows of G and X are read from HBM about once, where dealing units to the
+// pairs in turn spreads a group's tiles over pairs that reach them at different times.  Groups
+// go, largest first, to the team that would finish them first (modelled time: rounds x
+// (rows / 128 + 1.5) stages; ties to the lower team).  Every CTA computes the same
+// assignment; warp 0 calls it, lane q holding team q.
+__device__ void assign_teams(int E, int T, int P, const int32_t* msize, uint8_t* team_of) {
+    const int lane = threadIdx.x & 31;
+    const int full = P / T, b = P - full * T;
+    const int nteams = full + (b > 0 ? 1 : 0);
+    const float rounds = lane < full ? 1.f : static_cast<float>((T + b - 1) / max(b, 1));
+    float fin = 0.f;
+    for (int i = 0; i < E; ++i) {
+        const float cost = rounds * (static_cast<float>(msize[i]) * (1.f / 128.f) + 1.5f);
+        float v = lane < nteams ? fin + cost : 3.0e38f;
+        int who = lane;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+            const int w2 = __shfl_xor_sync(0xffffffffu, who, o);
+            if (v2 < v || (v2 == v && w2 < who)) { v = v2; who = w2; }
+        }
+        if (lane == who) fin += cost;
+        if (lane == 0) team_of[i] = static_cast<uint8_t>(who);
     }
 }
 
@@ -450,6 +484,97 @@ __device__ __forceinline__ Tile decode_unit(const GemmParams& p, Cursor& cu, con
     }
     t.nkb = (t.nred + kBK - 1) / kBK;
     return t;
+}
+
+// The units of one CTA pair, in the order it runs them: units pair, pair + pairs, ... of the
+// group-by-group numbering (decode_unit), or, with teams, the tiles of the groups its team
+// runs.  Every role of both CTAs walks the same sequence.
+struct Walker {
+    Cursor cu;
+    int u, pair, npairs, total;
+    bool teams;
+    const SmemCtl* c;
+    int my_team, slot, tsize, rounds, last;   // team geometry (tsize = pairs of the team)
+    int pos, e, s, m, r, off, npos;
+    int32_t na, nb;                           // offsets of the team's next group, loaded ahead
+};
+
+// The next group of the team at or after position from (E if none).
+__device__ __forceinline__ int team_next(const SmemCtl* c, int E, int team, int from) {
+    while (from < E && c->team_of[from] != team) ++from;
+    return from;
+}
+
+template <int OP, int RT>
+__device__ __forceinline__ void walker_init(Walker& w, const GemmParams& p, const Shape& sh,
+                                            const SmemCtl* c, bool sorted, int pair, int npairs,
+                                            int total) {
+    w.u = pair;
+    w.pair = pair;
+    w.npairs = npairs;
+    w.total = total;
+    w.c = c;
+    w.teams = OP == OP_WGRAD && sorted && p.teams;
+    if (!w.teams) {
+        cursor_init<OP, RT>(w.cu, p, sh, sorted ? c->order : nullptr);
+        return;
+    }
+    const int T = sh.ft, full = npairs / T, b = npairs - full * T;
+    w.my_team = pair / T;                      // == full for the remainder team
+    w.slot = pair - w.my_team * T;
+    w.tsize = w.my_team < full ? T : b;
+    w.rounds = w.my_team < full ? 1 : (T + b - 1) / b;
+    w.last = T - (w.rounds - 1) * w.tsize;     // tiles in the last round
+    w.off = 0;
+    w.r = w.rounds;                            // no group yet
+    w.pos = -1;
+    w.npos = team_next(c, p.E, w.my_team, 0);
+    if (w.npos < p.E) group_raw(p.offs, p.offs_kind, c->order[w.npos], w.na, w.nb);
+}
+
+template <int OP, int RT>
+__device__ __forceinline__ bool walker_next(Walker& w, const GemmParams& p, const Shape& sh,
+                                            Tile& t) {
+    if (!w.teams) {
+        if (w.u >= w.total) return false;
+        t = decode_unit<OP, RT>(p, w.cu, sh, w.u);
+        w.u += w.npairs;
+        return true;
+    }
+    for (;;) {
+        if (w.r < w.rounds) {
+            // Round r: the team's slots take tiles r * tsize + (slot - off) mod tsize; in the last
+            // round only the first `last` of them exist.  off turns by `last` from one group to
+            // the next, so the idle slots of the remainder team take turns.
+            int s2 = w.slot - w.off;
+            if (s2 < 0) s2 += w.tsize;
+            const int tile = w.r * w.tsize + s2;
+            ++w.r;
+            if (tile >= sh.ft) continue;
+            const int nt = static_cast<int>(sh.kt_div.div(static_cast<uint32_t>(tile)));
+            const int kt = tile - nt * sh.kt;
+            t.u = -1;
+            t.e = w.e;
+            t.f0 = nt * kPairM;
+            t.c0 = kt * kBN;
+            t.ncols = min(kBN, p.K - t.c0);
+            t.r0 = w.s;
+            t.nred = w.m;
+            t.nkb = (t.nred + kBK - 1) / kBK;
+            return true;
+        }
+        if (w.pos >= 0) {                      // the team's next group: turn the idle slots
+            w.off += w.last;
+            if (w.off >= w.tsize) w.off -= w.tsize;
+        }
+        w.pos = w.npos;
+        if (w.pos >= p.E) return false;
+        w.e = w.c->order[w.pos];
+        group_clamp(w.na, w.nb, p.rows, w.s, w.m);
+        w.npos = team_next(w.c, p.E, w.my_team, w.pos + 1);
+        if (w.npos < p.E) group_raw(p.offs, p.offs_kind, w.c->order[w.npos], w.na, w.nb);
+        w.r = 0;
+    }
 }
 
 // fwd / dgrad: MMA N (rows of the tile rounded up to 16), each CTA's half of it, and the
@@ -593,13 +718,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 5; ++i) prefetch_tmap(&p.tmB[i]);
     }
     const bool sorted = OP == OP_WGRAD && p.sort_groups && p.E <= kMaxSorted;
-    if (sorted) sort_groups_by_size(p, c->order);
+    if (sorted) sort_groups_by_size(p, c->order, c->msize);
     const int total = count_units<OP, RT>(p, sh, c->warp_tot);   // its __syncthreads publishes order
-    Cursor cu;
-    cursor_init<OP, RT>(cu, p, sh, sorted ? c->order : nullptr);
+    if (sorted && p.teams && warp == 0) assign_teams(p.E, sh.ft, npairs, c->msize, c->team_of);
     // Both CTAs' barriers are initialised (and the peer has started) before any CTA signals
-    // the other's barriers or allocates TMEM together with it.
+    // the other's barriers or allocates TMEM together with it; the cluster barrier also
+    // publishes the team assignment to the CTA's threads.
     cluster_sync();
+    Walker wk;
+    walker_init<OP, RT>(wk, p, sh, c, sorted, pair, npairs, total);
     if (warp == 2) {
         tmem_alloc_pair(&c->tmem_base, kTmemCols);
         tmem_relinquish_pair();
@@ -616,19 +743,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int stage = 0, jt = 0;   // jt: units with a tail step so far
             uint32_t phase = 0;
             bool ok = true;
-            for (int u = pair; u < total && ok; u += npairs) {
-                const Tile t = decode_unit<OP, RT>(p, cu, sh, u);
+            Tile t;
+            for (int j = 0; ok && walker_next<OP, RT>(wk, p, sh, t); ++j) {
                 int n_mma = 0, half = 0, bi = 0;
                 if (OP != OP_WGRAD) row_split(t.ncols, n_mma, half, bi);
                 const uint32_t bytes = (OP == OP_WGRAD)
                                            ? 2u * (kABytes + R::kBBytes)
                                            : 2u * (kABytes + (8u << bi) * 256u);
                 const int fa = t.f0 + kBM * static_cast<int>(pr.rank);   // this CTA's A rows
-                if (OP == OP_WGRAD && (EPI == EPI_FP32_ACC || EPI == EPI_BF16_ACC) &&
-                    p.prefetch && fa + kBM <= p.N)
-                    // The epilogue reads this CTA's 128 x 256 block of out after the unit's
-                    // mainloop: start bringing it into L2 now (whole 128-row blocks only).
-                    tma_prefetch_3d(&p.tmPre, t.c0, fa, t.e);
                 if (OP == OP_WGRAD) {
                     const int v = tail_rows(t.nred, t.nkb);
                     if (v) {
@@ -658,7 +780,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (even) mbar_arrive_expect_tx(&c->full[stage], bytes);
                     // Failure-detection test: the stage's barrier never completes, so the MMA
                     // issuer's bounded wait runs out and the pair aborts.
-                    if (p.test_withhold && pair == 0 && even && u == pair && kb == 0) {
+                    if (p.test_withhold && pair == 0 && even && j == 0 && kb == 0) {
                         if (++stage == R::kStages) { stage = 0; phase ^= 1u; }
                         continue;
                     }
@@ -705,8 +827,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             Acq acq;
             bool ok = true;
-            for (int u = pair; u < total && ok; u += npairs) {
-                const Tile t = decode_unit<OP, RT>(p, cu, sh, u);
+            Tile t;
+            while (ok && walker_next<OP, RT>(wk, p, sh, t)) {
                 const int nch = chunks_of<OP, EPI>(t.nkb);
                 const int A = nextb, B = nextb ^ 1;
                 if (nch > 1) {
@@ -797,8 +919,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // the even CTA's MMA.
         if (OP == OP_WGRAD) {
             int jt = 0;
-            for (int u = pair; u < total; u += npairs) {
-                const Tile t = decode_unit<OP, RT>(p, cu, sh, u);
+            Tile t;
+            while (walker_next<OP, RT>(wk, p, sh, t)) {
                 const int v = tail_rows(t.nred, t.nkb);
                 if (!v) continue;
                 const int tb = jt & 1;
@@ -826,8 +948,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // boxes of 32 rows x 64 bytes (32 bf16 or 16 fp32 columns): TMEM -> registers (one row
         // per thread) -> shared memory (64-byte swizzle) -> registers in line order (4 threads
         // per 64-byte row piece) -> coalesced global stores.  With accumulate the old
-        // values are loaded in the same line order (after an L2 prefetch of the block issued
-        // when the unit's loads started) and added there.
+        // values are loaded in the same line order, a few boxes ahead, and added there.  (An
+        // L2 prefetch of the unit's output block at the start of its mainloop was dropped:
+        // the prefetched lines were often evicted before the epilogue read them, so the
+        // wgrad-heavy accumulate read main_grad from HBM twice.)
         const int q = warp & 3, ew = warp - 4;          // TMEM lanes [32q, 32q + 32)
         const int hc = ew >> 2;                         // columns [128 hc, 128 hc + 128)
         const int mrow0 = kBM * static_cast<int>(pr.rank) + q * 32;   // first row of the pair tile
@@ -843,8 +967,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool ok = true;
         int nextb = 0;
         Acq acq;                        // the MMA issuer's buffer plan, followed step by step
-        for (int u = pair; u < total && ok; u += npairs) {
-            const Tile t = decode_unit<OP, RT>(p, cu, sh, u);
+        Tile t;
+        while (ok && walker_next<OP, RT>(wk, p, sh, t)) {
             const int nch = chunks_of<OP, EPI>(t.nkb);
             const int A = nextb, B = nextb ^ 1;
             const uint32_t lanebase = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -868,7 +992,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // chunk is all in or all out) is neither read nor written; the split form's partial
             // tiles are written whole.
             constexpr int kBoxCols = f32 ? 16 : 32;
-            constexpr int kPer = 32 / kBoxCols;             // boxes per 32 TMEM columns
             constexpr int kBoxes = 128 / kBoxCols;
             constexpr int kAhead = acc ? 3 : 1;
             constexpr int kChunkCols = 16 / osz;
@@ -932,20 +1055,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 acq.bump(A);
             }
             const uint32_t taddr = lanebase + static_cast<uint32_t>(fb * kBN + 128 * hc);
-            uint32_t r[32];
+            uint32_t r[kBoxCols];       // one box's columns: TMEM is read box by box
 #pragma unroll
             for (int b = 0; b < kBoxes; ++b) {
                 if (b >= nbox) break;
-                const int h = b % kPer;
-                if (h == 0) {
+                {
                     if (t.nkb > 0) {
-                        tmem_ld_32x32b_x32(taddr + b * kBoxCols, r);
+                        if constexpr (f32) tmem_ld_32x32b_x16(taddr + b * kBoxCols, r);
+                        else tmem_ld_32x32b_x32(taddr + b * kBoxCols, r);
                         tmem_ld_wait();
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = 0u;   // +0.0f: empty group
+                        for (int j = 0; j < kBoxCols; ++j) r[j] = 0u;   // +0.0f: empty group
                     }
-                    if (b + kPer >= nbox) {
+                    if (b + 1 >= nbox) {
                         // Every TMEM column of the unit is in registers: hand the buffer back
                         // to the MMA before the remaining stores.
                         tc_fence_before();
@@ -961,7 +1084,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int g = 0; g < 4; ++g) {
                     uint4 v;
                     if constexpr (f32) {
-                        const uint32_t* w = r + 16 * h + 4 * g;
+                        const uint32_t* w = r + 4 * g;
                         v = make_uint4(w[0], w[1], w[2], w[3]);
                     } else {
                         const uint32_t* w = r + 8 * g;
@@ -1028,9 +1151,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int hc = (warp - 4) >> 2;         // columns [128 hc, 128 hc + 128)
         const int mrow = kBM * static_cast<int>(pr.rank) + q * 32 + lane;   // row of the pair tile
         const uint32_t tempty0 = mapa_shared(smem_u32(&c->tempty[0]), 0u);
-        int it = 0;
-        for (int u = pair; u < total; u += npairs, ++it) {
-            const Tile t = decode_unit<OP, RT>(p, cu, sh, u);
+        Tile t;
+        for (int it = 0; walker_next<OP, RT>(wk, p, sh, t); ++it) {
             const int buf = it & 1;
             if (!wait_bar_warp(&c->tfull[buf], (it >> 1) & 1, c, pr, p.err)) break;
             tc_fence_after();
