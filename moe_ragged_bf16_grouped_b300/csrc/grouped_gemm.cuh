@@ -1005,6 +1005,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint4 old[kAhead][4];
             auto first_loads = [&]() {
                 if constexpr (acc) {
+                    // The whole row segment of this thread's TMEM lane into L2 (up to 4 lines),
+                    // before the unit's MMAs finish: the boxes past the first kAhead then find
+                    // their old values in L2 instead of HBM.
+                    if (lane < nvalid) {
+                        const uint8_t* prow = obase + static_cast<size_t>(lane) * ldo + (128 * hc) * osz;
+                        const int seg = min(128, kvalid) * osz;       // bytes of the row segment
+                        for (int o = 0; o < seg; o += 128) prefetch_l2(prow + o);
+                    }
 #pragma unroll
                     for (int b = 0; b < kAhead; ++b)
                         if (b < nbox)

@@ -59,6 +59,11 @@ __device__ __forceinline__ void red_add_v4_f32(void* ptr, uint4 v) {
                  : "memory");
 }
 
+// Asks L2 to fetch the line holding ptr (a hint: nothing is returned).
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA / tensor core) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
