@@ -261,7 +261,7 @@ def pick_peak(clocks, timed_ms, burst, sustained):
 def _oracle_probe(w, d, ops, target_s, rng):
     """Times the fp64 oracle on a bounded sample of the workload: rows of Y / dX and rows
     (e, n, all k) of dW of up to four non-empty groups, each as a one-group problem copied to
-    the host.  Returns (GFLOP/s, cores, description)."""
+    the host.  Returns (GFLOP/s over the sample, GFLOP/s per op kind, cores, description)."""
     import oracle
     sizes = d["sizes"]
     st = np.concatenate([[0], np.cumsum(sizes)[:-1]])
@@ -278,33 +278,40 @@ def _oracle_probe(w, d, ops, target_s, rng):
         host.append(g)
 
     def run(n):
-        t0, fl = time.perf_counter(), 0.0
+        """Seconds and FLOPs of each op kind over the sample."""
+        t, fl = {k: 0.0 for k in ops}, {k: 0.0 for k in ops}
         for g in host:
             ids = rng.integers(0, g["m"], n).astype(np.int64)
-            if "fwd" in ops:
-                oracle.fwd_rows(g["X"], g["W"], g["one"], ids)
-                fl += 2.0 * w.N * w.K * n
-            if "dgrad" in ops:
-                oracle.dgrad_rows(g["G"], g["W"], g["one"], ids)
-                fl += 2.0 * w.N * w.K * n
-            if "wgrad" in ops:
-                ns = rng.integers(0, w.N, n)
-                oracle.wgrad_rows(g["G"], g["X"], g["one"], 1, w.N, w.K,
-                                  np.stack([np.zeros_like(ns), ns], 1))
-                fl += 2.0 * g["m"] * w.K * n
-        return time.perf_counter() - t0, fl
+            for kind in ops:
+                t0 = time.perf_counter()
+                if kind == "fwd":
+                    oracle.fwd_rows(g["X"], g["W"], g["one"], ids)
+                    fl[kind] += 2.0 * w.N * w.K * n
+                elif kind == "dgrad":
+                    oracle.dgrad_rows(g["G"], g["W"], g["one"], ids)
+                    fl[kind] += 2.0 * w.N * w.K * n
+                else:
+                    ns = rng.integers(0, w.N, n)
+                    oracle.wgrad_rows(g["G"], g["X"], g["one"], 1, w.N, w.K,
+                                      np.stack([np.zeros_like(ns), ns], 1))
+                    fl[kind] += 2.0 * g["m"] * w.K * n
+                t[kind] += time.perf_counter() - t0
+        return t, fl
 
     n = max(1, oracle.num_threads() // len(host))
     while True:
-        dt, fl = run(n)
+        t, fl = run(n)
+        dt = sum(t.values())
         if dt >= target_s / 4 or n >= 1 << 12:
             break
         n *= 2
     n = max(1, int(n * target_s / max(dt, 1e-3)))
-    dt, fl = run(n)
+    t, fl = run(n)
+    dt = sum(t.values())
     desc = (f"{n} sampled outputs per op ({', '.join(ops)}) in each of groups {groups}, "
             f"one-group fp64 C oracle problems; {dt:.1f} s")
-    return fl / dt / 1e9, oracle.num_threads(), desc
+    per_op = {k: fl[k] / max(t[k], 1e-9) / 1e9 for k in ops}
+    return sum(fl.values()) / dt / 1e9, per_op, oracle.num_threads(), desc
 
 
 def time_configs(dev, peaks, iters, oracle_s, with_oracle):
@@ -380,10 +387,12 @@ def time_configs(dev, peaks, iters, oracle_s, with_oracle):
                  "nonempty_groups": int(np.count_nonzero(sizes)), "ops": ops}
         if with_oracle:
             kinds = [("wgrad" if o.startswith("wgrad") else o) for o in calls]
-            gf, cores, desc = _oracle_probe(w, d, kinds, oracle_s, rng)
+            kinds_u = list(dict.fromkeys(kinds))
+            gf, per_op, cores, desc = _oracle_probe(w, d, kinds_u, oracle_s, rng)
             entry["oracle"] = {"gflops": round(gf, 2), "cores": cores, "sample": desc,
+                               "gflops_per_op": {k: round(v, 2) for k, v in per_op.items()},
                                "full_op_s_extrapolated": {
-                                   o: round(rl.op_cost(k, sizes, w.N, w.K)[0] / (gf * 1e9), 1)
+                                   o: round(rl.op_cost(k, sizes, w.N, w.K)[0] / (per_op[k] * 1e9), 1)
                                    for o, k in zip(calls, kinds)}}
         if gdg.gdg_device_error() != 0:
             raise RuntimeError(f"device error word set during the {name} timings")

@@ -3,7 +3,8 @@ GEMM's arithmetic is here).
 
 FLOPs count the real rows of every group, 2 M N K with M the summed group sizes.  Bytes are what
 the operation must move at least once: fwd / dgrad read the packed rows and the weights of the
-non-empty experts and write the packed outputs, 2 (M K + E_ne N K + M N); wgrad reads G and X and
+non-empty experts and write the packed outputs, 2 (M K + E_ne N K + M N) for both (fwd reads
+M K and writes M N, dgrad reads M N and writes M K); wgrad reads G and X and
 writes dW, 2 (M K + M N) + E N K s_out, plus E N K s_out read again when it accumulates into an
 existing output.  The combined roofline is t_roof = max(FLOPs / P, bytes / BW).
 """
@@ -26,7 +27,8 @@ def op_cost(op: str, sizes, N: int, K: int, out_esize: int = 2, accumulate: bool
         nbytes = 2 * (M * K + M * N) + E * N * K * out_esize * (2 if accumulate else 1)
         wbytes = 0
     else:
-        nbytes = 2 * (M * K + e_ne * N * K + M * (N if op == "fwd" else K))
+        # fwd reads X [M, K] and writes Y [M, N]; dgrad reads G [M, N] and writes dX [M, K]
+        nbytes = 2 * (M * K + e_ne * N * K + M * N)
         wbytes = 2 * e_ne * N * K
     return flops, float(nbytes), float(wbytes)
 

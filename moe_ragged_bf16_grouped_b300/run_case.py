@@ -112,7 +112,7 @@ def main():
         s_out = out.element_size()
         nbytes = 2 * (M * w.K + M * w.N) + w.E * w.N * w.K * s_out * (2 if acc else 1)
     else:
-        nbytes = 2 * (M * w.K + e_ne * w.N * w.K + M * (w.N if args.op == "fwd" else w.K))
+        nbytes = 2 * (M * w.K + e_ne * w.N * w.K + M * w.N)   # fwd and dgrad alike
     line["bytes"] = nbytes
     line["gbs"] = nbytes / med / 1e6 if ts else None
     peaks_path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),

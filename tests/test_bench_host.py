@@ -37,6 +37,7 @@ def test_algorithmic_costs_of_the_workloads():
     assert f == 2.0 * 16384 * 14336 * 4096                     # 1.924 TFLOP
     assert b == 2 * (16384 * 4096 + 8 * 14336 * 4096 + 16384 * 14336)
     assert wb == 2 * 8 * 14336 * 4096
+    assert rl.op_cost("dgrad", sizes, 14336, 4096) == (f, b, wb)   # reads G [M, N], writes dX [M, K]
     dec = wl.sizes_decode(0)
     e_ne = int(np.count_nonzero(dec))
     f, b, wb = rl.op_cost("fwd", dec, 2048, 7168)
