@@ -249,9 +249,12 @@ int sort_groups_rule(int64_t rows, int E) {
 int32_t auto_split_rows(int64_t rows, int E, int N, int K) {
     const int64_t tpe = tiles_per_expert(N, K);
     // Shapes with few output tiles leave SMs idle in the unsplit form; cut the rows of
-    // each group into fixed chunks instead.  The rule looks at shapes only, so the
-    // bits never depend on the GPU it runs on.
-    if (rows <= 0 || static_cast<int64_t>(E) * tpe >= 64) return -1;
+    // each group into fixed chunks instead, when the groups are long enough (6144 rows on
+    // average) for the shorter units to repay the ordered reduce: measured, 8192-row groups
+    // gain 17 % (E = 2, N = K = 1024) and 4096-row groups lose 6-14 % (E = 8, N = K = 512).
+    // The rule looks at shapes only, so the bits never depend on the GPU it runs on.
+    if (rows <= 0 || static_cast<int64_t>(E) * tpe >= 64 || rows < static_cast<int64_t>(E) * 6144)
+        return -1;
     int64_t r = ceil_div(rows * tpe, 128);
     r = ceil_div(r, 64) * 64;
     if (r < 128) r = 128;

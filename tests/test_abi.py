@@ -151,9 +151,10 @@ def test_workspace_bytes_and_auto_form(lib):
     # the automatic form depends on shapes only
     assert g(16384, 8, 14336, 4096) == -1          # many tiles: unsplit
     assert g(65536, 64, 1536, 2048) == -1
-    r = g(512, 4, 256, 256)
+    assert g(512, 4, 256, 256) == -1              # few tiles but short groups: unsplit
+    r = g(65536, 4, 256, 256)                      # few tiles, long groups: split
     assert r > 0 and r % 64 == 0
-    assert f(2, 512, 4, 256, 256, 0, 0, 0) == f(2, 512, 4, 256, 256, 0, 0, r)
+    assert f(2, 65536, 4, 256, 256, 0, 0, 0) == f(2, 65536, 4, 256, 256, 0, 0, r) > 0
 
 
 def test_status_strings(lib):
@@ -188,3 +189,10 @@ def test_plan_refusals_leave_no_plan(lib):
     assert lib.gdg_plan_create(0, ctypes.byref(good()), OFFS, 4, 256, 256, 0, 0, None) == EINVAL
     assert lib.gdg_plan_launch(None, None) == EINVAL
     lib.gdg_plan_destroy(None)
+
+
+def test_async_error_read_refuses_null_destination(lib):
+    f = lib.gdg_device_error_async
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    assert f(None, None) == EINVAL          # refused before any CUDA call

@@ -71,3 +71,27 @@ def test_withheld_stage_times_out_and_context_survives(cuda_lib, op):
     torch.cuda.synchronize()
     assert cuda_lib.gdg_device_error() == 0
     assert np.isfinite(waited)
+
+
+def test_error_word_read_on_a_stream_without_host_sync(cuda_lib):
+    """gdg_device_error_async copies the word into pinned host memory (and resets it) in stream
+    order: after a withheld stage the copy holds GDG_ETIMEOUT, a second read 0; a device-side
+    destination works the same way."""
+    w = wl.Workload("withhold_async", E=2, N=256, K=256, ops=(), main_grad_std=1.0)
+    h, d = inputs_on(w, DEV, seed=6, sizes=[200, 300], kind=wl.OFFS_ENDS)
+    assert cuda_lib.gdg_device_error() == 0
+    args, dims, _, keep = cuda_lib._fwd_args(d["X"], d["W"], d["offs"], None, wl.OFFS_ENDS)
+    stream = torch.cuda.current_stream()
+    host = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+    dev_word = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    assert withhold(cuda_lib, cuda_lib.GDG_OP_FWD, args, dims, d["offs"]) == 0
+    cuda_lib.gdg_device_error_async(host, stream=stream)   # enqueued behind the launch
+    stream.synchronize()
+    del keep
+    assert int(host.item()) == GDG_ETIMEOUT
+    cuda_lib.gdg_device_error_async(dev_word, stream=stream)
+    assert int(dev_word.item()) == 0                        # the first read reset it
+    cuda_lib.grouped_det_gemm_fwd(d["X"], d["W"], d["offs"])
+    cuda_lib.gdg_device_error_async(host, stream=stream)
+    stream.synchronize()
+    assert int(host.item()) == 0

@@ -76,7 +76,7 @@ CASES = [
     # sizes, split_rows
     ([900, 0, 1, 333, 64, 2600, 17], 128),
     ([900, 0, 1, 333, 64, 2600, 17], 64),
-    ([4096, 4096], 0),                 # the automatic split (E * tiles per expert < 64)
+    ([7000, 6500], 0),                 # the automatic split (few tiles, long groups)
     ([3000, 5, 0, 2500], 2304),        # chunks longer than 2048 rows (fp32 chunking inside)
 ]
 
