@@ -164,7 +164,10 @@ GDG_API gdg_status grouped_det_gemm_wgrad(const gdg_args* args, const int32_t* o
 GDG_API size_t grouped_det_gemm_workspace_bytes(int op, int64_t rows, int E, int N, int K,
                                         gdg_dtype out_dtype, int accumulate, int32_t split_rows);
 
-/* The split_rows value that split_rows == 0 resolves to for these shapes (-1 = unsplit). */
+/* The split_rows value that split_rows == 0 resolves to for these shapes (-1 = unsplit).
+ * A split is chosen only when the output has fewer than 64 tiles of 256 x 256
+ * (E * ceil(N/256) * ceil(K/256) < 64) and rows >= 6144 * E; it depends on the shapes
+ * alone, never on the device.  -1 also for invalid arguments. */
 GDG_API int32_t grouped_det_gemm_auto_split_rows(int64_t rows, int E, int N, int K);
 
 /* Static text for a status code. */
