@@ -406,8 +406,10 @@ __device__ __forceinline__ void cursor_seek(Cursor& cu, const GemmParams& p, con
 // round to nearest even, in chunk order) into a running sum kept in the other TMEM buffer.
 constexpr int kChunkStages = 16;
 
-// Times each of the two TMEM buffers has been handed to the epilogue (its tfull / tempty
-// phase count), in registers.
+// Per TMEM buffer, in registers: on the MMA issuer, the uses of the buffer so far, each ended
+// by one tempty phase; on the epilogue warps, the tfull phases of the buffer waited for so far.
+// The two differ by the running-sum uses of chunked units, which the epilogue warps take
+// without a tfull phase.
 struct Acq {
     uint32_t n0 = 0, n1 = 0;
     __device__ __forceinline__ uint32_t of(int b) const { return b ? n1 : n0; }
@@ -819,9 +821,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer (even CTA)
         // One thread waits, issues and commits; the other lanes of the warp stay idle.
-        // TMEM buffers alternate between units; acq counts the times each buffer has been
-        // handed to the epilogue (its tfull / tempty phase).  A chunked unit keeps buffer A
-        // for its chunks and hands buffer B to the epilogue for the running sum.
+        // TMEM buffers alternate between units; acq counts the uses of each buffer (its
+        // tempty phases).  A chunked unit keeps buffer A for its chunks and leaves buffer B to
+        // the epilogue warps for the running sum.
         if (even && lane == 0) {
             int stage = 0, nextb = 0, jt = 0;   // jt: units with a tail step so far
             uint32_t phase = 0;
@@ -832,11 +834,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int nch = chunks_of<OP, EPI>(t.nkb);
                 const int A = nextb, B = nextb ^ 1;
                 if (nch > 1) {
-                    // The running-sum buffer: once its previous use is drained, hand it over
-                    // (the commit arrives when every MMA issued so far is done).
-                    if (!wait_bar(&c->tempty[B], (acq.of(B) & 1u) ^ 1u, c, pr, p.err)) { ok = false; break; }
-                    tc_fence_after();
-                    umma_commit_pair(&c->tfull[B], 3);
+                    // The running sum is a use of B that no MMA writes: the epilogue warps
+                    // start it once they are done with B's previous use (each warp touches only
+                    // its own lanes and columns, in order), so the chunks' MMAs need not wait
+                    // for that use to drain.  Its end is a tempty[B] phase like any other.  By
+                    // the time this thread waits on tempty[B] again, the phase before this use
+                    // has completed: chunk 1 waits for chunk 0's fold, which every epilogue
+                    // warp starts only after it has released B's previous use.
                     acq.bump(B);
                 }
                 int n_mma = kBN, half = 0, bi = 0;
@@ -966,7 +970,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int wsw = (lane >> 1) & 3;                // 64-byte swizzle: chunk g at g ^ wsw
         bool ok = true;
         int nextb = 0;
-        Acq acq;                        // the MMA issuer's buffer plan, followed step by step
+        Acq acq;                        // tfull phases waited for, per buffer
         Tile t;
         while (ok && walker_next<OP, RT>(wk, p, sh, t)) {
             const int nch = chunks_of<OP, EPI>(t.nkb);
@@ -1026,9 +1030,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int fb = A;                 // the buffer that ends up holding the unit's value
             if (nch > 1) {
                 // Chunked unit: B receives chunk 0, then B = RN(B + chunk c) for c = 1, 2, ...
-                if (!wait_bar_warp(&c->tfull[B], acq.of(B) & 1u, c, pr, p.err)) { ok = false; break; }
-                tc_fence_after();
-                acq.bump(B);
+                // No MMA writes B meanwhile, and this warp's own reads of B's previous use
+                // completed (tcgen05.wait::ld) before these stores, so B needs no barrier.
                 for (int ch = 0; ch < nch; ++ch) {
                     if (!wait_bar_warp(&c->tfull[A], acq.of(A) & 1u, c, pr, p.err)) { ok = false; break; }
                     tc_fence_after();
