@@ -497,13 +497,26 @@ struct Walker {
     bool teams;
     const SmemCtl* c;
     int my_team, slot, tsize, rounds, last;   // team geometry (tsize = pairs of the team)
-    int pos, e, s, m, r, off, npos;
+    int pos, e, s, m, r, off, npos, walk;
     int32_t na, nb;                           // offsets of the team's next group, loaded ahead
 };
 
-// The next group of the team at or after position from (E if none).
-__device__ __forceinline__ int team_next(const SmemCtl* c, int E, int team, int from) {
-    while (from < E && c->team_of[from] != team) ++from;
+// The order in which a team visits the size-sorted list: step j of the walk looks at position
+// walk_pos(j).  A full team alternates between the largest and the smallest groups left
+// (kWalkAlternate), so that the epilogue writes out a short group's tiles while the MMAs of a
+// long group run; the remainder team goes from the smallest group up (kWalkAscending), so that
+// its output writes fall while the full teams run long groups.  The order changes only when a
+// tile runs, never what it computes.
+enum Walk : int { kWalkAlternate = 0, kWalkAscending = 1 };
+
+__device__ __forceinline__ int walk_pos(int j, int E, int walk) {
+    if (walk == kWalkAscending) return E - 1 - j;
+    return (j & 1) ? E - 1 - (j >> 1) : (j >> 1);
+}
+
+// The first step at or after from whose group belongs to the team (E if none).
+__device__ __forceinline__ int team_next(const SmemCtl* c, int E, int team, int from, int walk) {
+    while (from < E && c->team_of[walk_pos(from, E, walk)] != team) ++from;
     return from;
 }
 
@@ -530,8 +543,9 @@ __device__ __forceinline__ void walker_init(Walker& w, const GemmParams& p, cons
     w.off = 0;
     w.r = w.rounds;                            // no group yet
     w.pos = -1;
-    w.npos = team_next(c, p.E, w.my_team, 0);
-    if (w.npos < p.E) group_raw(p.offs, p.offs_kind, c->order[w.npos], w.na, w.nb);
+    w.walk = w.my_team < full ? kWalkAlternate : kWalkAscending;
+    w.npos = team_next(c, p.E, w.my_team, 0, w.walk);
+    if (w.npos < p.E) group_raw(p.offs, p.offs_kind, c->order[walk_pos(w.npos, p.E, w.walk)], w.na, w.nb);
 }
 
 template <int OP, int RT>
@@ -571,10 +585,11 @@ __device__ __forceinline__ bool walker_next(Walker& w, const GemmParams& p, cons
         }
         w.pos = w.npos;
         if (w.pos >= p.E) return false;
-        w.e = w.c->order[w.pos];
+        w.e = w.c->order[walk_pos(w.pos, p.E, w.walk)];
         group_clamp(w.na, w.nb, p.rows, w.s, w.m);
-        w.npos = team_next(w.c, p.E, w.my_team, w.pos + 1);
-        if (w.npos < p.E) group_raw(p.offs, p.offs_kind, w.c->order[w.npos], w.na, w.nb);
+        w.npos = team_next(w.c, p.E, w.my_team, w.pos + 1, w.walk);
+        if (w.npos < p.E)
+            group_raw(p.offs, p.offs_kind, w.c->order[walk_pos(w.npos, p.E, w.walk)], w.na, w.nb);
         w.r = 0;
     }
 }
