@@ -314,9 +314,12 @@ def _oracle_probe(w, d, ops, target_s, rng):
     return sum(fl.values()) / dt / 1e9, per_op, oracle.num_threads(), desc
 
 
-def time_configs(dev, peaks, iters, oracle_s, with_oracle):
+def time_configs(dev, peaks, iters, oracle_s, with_oracle, pause):
     """Every workload of the path, each op timed alone: median of `iters` launches, each after a
-    512 MiB L2 flush, CUDA events on the launching stream."""
+    512 MiB L2 flush and `pause` seconds of idle GPU, CUDA events on the launching stream.  The
+    pause lets the power controller bring the SM clock back between launches, so that each
+    launch runs as a kernel timed alone does, which is the condition of the burst peak the
+    fractions use; back to back, the heavier launches run at power-capped clocks."""
     import moe_ragged_bf16_grouped_b300 as gdg
     P = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     BW = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -355,6 +358,9 @@ def time_configs(dev, peaks, iters, oracle_s, with_oracle):
                 fn()
             ts = []
             for _ in range(iters):
+                if pause > 0:
+                    torch.cuda.synchronize(dev)
+                    time.sleep(pause)
                 flush.fill_(1)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
@@ -399,7 +405,8 @@ def time_configs(dev, peaks, iters, oracle_s, with_oracle):
         result[name] = entry
         del d, calls
         torch.cuda.empty_cache()
-    return {"timing": f"median of {iters} launches per op, each after a 512 MiB L2 flush; "
+    return {"timing": f"median of {iters} launches per op, each after {pause} s of idle GPU and "
+                      f"a 512 MiB L2 flush; "
                       f"roofline against the measured burst bf16 rate {P} TFLOP/s and copy "
                       f"bandwidth {BW} GB/s, and against the nominal 2250 TFLOP/s, 8000 GB/s",
             "configs": result}
@@ -581,7 +588,7 @@ def run_ours(args, world, rank, local):
            "roofline": roofline}
     if rank == 0 and not args.no_per_config:
         out["per_config"] = time_configs(dev, peaks, args.config_iters, args.config_oracle_s,
-                                         not args.no_cpu_baseline)
+                                         not args.no_cpu_baseline, args.config_pause)
     if rank == 0:
         if not args.no_cpu_baseline:
             h = {"X": X, "G": G, "W": W}
@@ -640,6 +647,8 @@ def main():
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-workload op timings (the headline step only)")
     ap.add_argument("--config-iters", type=int, default=10)
+    ap.add_argument("--config-pause", type=float, default=0.1,
+                    help="idle seconds before each per-config launch (power controller recovery)")
     ap.add_argument("--config-oracle-s", type=float, default=3.0,
                     help="oracle seconds per workload in the per-config timings")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
