@@ -315,11 +315,12 @@ def _oracle_probe(w, d, ops, target_s, rng):
 
 
 def time_configs(dev, peaks, iters, oracle_s, with_oracle, pause):
-    """Every workload of the path, each op timed alone: median of `iters` launches, each after a
-    512 MiB L2 flush and `pause` seconds of idle GPU, CUDA events on the launching stream.  The
-    pause lets the power controller bring the SM clock back between launches, so that each
-    launch runs as a kernel timed alone does, which is the condition of the burst peak the
-    fractions use; back to back, the heavier launches run at power-capped clocks."""
+    """Every workload of the path, each op timed alone: median of `iters` launches, CUDA events on
+    the launching stream.  Before each timed launch: `pause` seconds of idle GPU, two untimed
+    launches of the same op and a 512 MiB L2 flush (ops shorter than 0.2 ms: the flush only).  The pause lets the power controller bring
+    the SM clock back (back to back, the heavier ops run at power-capped clocks), the two
+    launches bring the clocks up from idle, so that each timed launch runs as a kernel timed
+    alone does: the condition of the burst peak that the fractions use."""
     import moe_ragged_bf16_grouped_b300 as gdg
     P = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     BW = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -354,13 +355,23 @@ def time_configs(dev, peaks, iters, oracle_s, with_oracle, pause):
                 out.element_size(), acc)
         ops = {}
         for op, (fn, esz, acc) in calls.items():
-            for _ in range(3):
+            for _ in range(2):
                 fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            # A launch far shorter than the power controller's reaction time is not slowed by
+            # it, and the pause would only leave its clocks at idle: no pause for those.
+            op_pause = pause if a.elapsed_time(b) > 0.2 else 0.0
             ts = []
             for _ in range(iters):
-                if pause > 0:
+                if op_pause > 0:
                     torch.cuda.synchronize(dev)
-                    time.sleep(pause)
+                    time.sleep(op_pause)
+                    fn()
+                    fn()
                 flush.fill_(1)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
@@ -371,7 +382,7 @@ def time_configs(dev, peaks, iters, oracle_s, with_oracle, pause):
             ms = float(np.median(ts))
             kind = "wgrad" if op.startswith("wgrad") else op
             flops, nbytes, wbytes = rl.op_cost(kind, sizes, w.N, w.K, esz, acc)
-            r = {"ms": round(ms, 4), "ms_min": round(float(np.min(ts)), 4),
+            r = {"ms": round(ms, 4), "ms_min": round(float(np.min(ts)), 4), "pause_s": op_pause,
                  "tflops": round(flops / ms / 1e9, 1), "gbs": round(nbytes / ms / 1e6, 1),
                  "algorithmic_bytes": nbytes}
             roof = rl.roofline(ms, flops, nbytes, P, BW)
@@ -405,8 +416,9 @@ def time_configs(dev, peaks, iters, oracle_s, with_oracle, pause):
         result[name] = entry
         del d, calls
         torch.cuda.empty_cache()
-    return {"timing": f"median of {iters} launches per op, each after {pause} s of idle GPU and "
-                      f"a 512 MiB L2 flush; "
+    return {"timing": f"median of {iters} launches per op, each after {pause} s of idle GPU, two "
+                      f"untimed launches and a 512 MiB L2 flush (ops under 0.2 ms: the flush "
+                      f"only); "
                       f"roofline against the measured burst bf16 rate {P} TFLOP/s and copy "
                       f"bandwidth {BW} GB/s, and against the nominal 2250 TFLOP/s, 8000 GB/s",
             "configs": result}
