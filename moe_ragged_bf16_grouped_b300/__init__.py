@@ -27,7 +27,7 @@ __all__ = [
     "grouped_det_gemm_workspace_bytes", "grouped_det_gemm_auto_split_rows",
     "grouped_det_gemm_wgrad_noalloc", "GDG_NOALLOC_SCRATCH_BYTES", "GroupedDetGemmPlan",
     "prepare_grouped_det_gemm_fwd", "prepare_grouped_det_gemm_dgrad",
-    "prepare_grouped_det_gemm_wgrad", "grouped_det_mm", "GroupedDetMm",
+    "prepare_grouped_det_gemm_wgrad", "grouped_det_mm", "GroupedDetMm", "DeviceErrorWatch",
     "gdg_status_string", "gdg_device_error", "gdg_device_error_async", "library_path",
     "grouped_gemm_wgrad", "grouped_gemm_wgrad_workspace_bytes",
 ]
@@ -123,6 +123,55 @@ def gdg_device_error_async(dst: torch.Tensor, stream=None) -> torch.Tensor:
     if st != GDG_OK:
         raise GdgError(st, "gdg_device_error_async")
     return dst
+
+
+class DeviceErrorWatch:
+    """A check of one device's error word that never blocks the host.
+
+    ``arm(stream)`` enqueues on the stream a copy of the word into a slot of pinned host memory,
+    and its reset (``gdg_device_error_async``), and records an event behind them.  ``check()``
+    reads every armed slot whose event has completed, skipping the others, and raises
+    ``GdgError`` (``GDG_ETIMEOUT``: a launch stopped early and left its outputs unspecified) if
+    one of them held a set word.  A timed-out launch is therefore reported by the first
+    ``check()`` after the stream has passed the next ``arm()``, without any synchronisation.
+    Neither call does anything while the current stream is being captured into a graph."""
+
+    def __init__(self, device, slots: int = 8):
+        self.device = torch.device(device)
+        if self.device.type != "cuda":
+            raise ValueError("DeviceErrorWatch needs a CUDA device")
+        self._words = torch.zeros(slots, dtype=torch.int32).pin_memory()
+        self._events = [None] * slots
+        self._next = 0
+
+    def _read(self, i: int) -> None:
+        self._events[i] = None
+        word = int(self._words[i])
+        if word != GDG_OK:
+            self._words[i] = GDG_OK
+            raise GdgError(word, "device error word (DeviceErrorWatch)")
+
+    def check(self) -> None:
+        if torch.cuda.is_current_stream_capturing():
+            return
+        for i, ev in enumerate(self._events):
+            if ev is not None and ev.query():
+                self._read(i)
+
+    def arm(self, stream=None) -> None:
+        if torch.cuda.is_current_stream_capturing():
+            return
+        i = self._next
+        if self._events[i] is not None:      # every slot in flight: the oldest must land first
+            self._events[i].synchronize()
+            self._read(i)
+        self._next = (i + 1) % len(self._events)
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        gdg_device_error_async(self._words[i:i + 1], stream)
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        self._events[i] = ev
 
 
 def grouped_det_gemm_workspace_bytes(op: int, rows: int, E: int, N: int, K: int,

@@ -24,6 +24,11 @@ convention that the MoE grouped GEMM pull request adopts for the deterministic w
   non-reentrant checkpoints work like any autograd graph (the backward adds once).
 
 Without fusion, w's gradient is dW in w's dtype (bf16), under any checkpoint.
+
+Every backward arms a ``DeviceErrorWatch`` for its device after its launches, and every forward
+and backward first checks the watch: a launch whose in-kernel wait ran out (its outputs are
+unspecified) raises ``GdgError`` in a later call instead of letting training go on silently,
+with no host synchronisation.
 """
 from __future__ import annotations
 
@@ -80,6 +85,21 @@ def _in_checkpoint_recompute() -> bool:
     return False
 
 
+_watches = {}
+
+
+def _watch(device: torch.device):
+    """The error watch of this device (one per device, created on first use); None off CUDA
+    (the library refuses such tensors itself)."""
+    if device.type != "cuda":
+        return None
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    w = _watches.get(key)
+    if w is None:
+        w = _watches[key] = _gdg.DeviceErrorWatch(torch.device("cuda", key))
+    return w
+
+
 def _refuse_tracing():
     if torch.jit.is_tracing() or torch.compiler.is_compiling():
         raise NotImplementedError("grouped_det_mm cannot be traced or compiled")
@@ -103,6 +123,9 @@ class GroupedDetMm(torch.autograd.Function):
             # without main_grad.
             if not (getattr(w, "main_grad", None) is None and _in_checkpoint_recompute()):
                 _check_main_grad(w)
+        watch = _watch(x.device)
+        if watch is not None:
+            watch.check()
         y = _gdg.grouped_det_gemm_fwd(x, w, offs)
         ctx.save_for_backward(x, w, offs)
         ctx.fuse = fuse_wgrad_accumulation
@@ -118,6 +141,9 @@ class GroupedDetMm(torch.autograd.Function):
         if torch.is_grad_enabled():
             raise NotImplementedError("grouped_det_mm does not support create_graph")
         x, w, offs = ctx.saved_tensors
+        watch = _watch(x.device)
+        if watch is not None:
+            watch.check()
         dy = dy.contiguous()
         dx = dw = None
         if ctx.needs_input_grad[0]:
@@ -135,6 +161,10 @@ class GroupedDetMm(torch.autograd.Function):
                         dw = torch.empty(w.shape, dtype=w.dtype, device=w.device)
             else:
                 dw = _gdg.grouped_det_gemm_wgrad(dy, x, offs, out_dtype=w.dtype)
+        # The forward's launch and this backward's are behind this point on the stream.
+        if watch is not None:
+            with torch.cuda.device(x.device):
+                watch.arm()
         return dx, dw, None, None
 
 

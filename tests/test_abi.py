@@ -196,3 +196,10 @@ def test_async_error_read_refuses_null_destination(lib):
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
     assert f(None, None) == EINVAL          # refused before any CUDA call
+
+
+def test_error_watch_needs_a_cuda_device():
+    """DeviceErrorWatch reads the device error word of a CUDA device only."""
+    import moe_ragged_bf16_grouped_b300 as gdg
+    with pytest.raises(ValueError):
+        gdg.DeviceErrorWatch("cpu")

@@ -95,3 +95,46 @@ def test_error_word_read_on_a_stream_without_host_sync(cuda_lib):
     cuda_lib.gdg_device_error_async(host, stream=stream)
     stream.synchronize()
     assert int(host.item()) == 0
+
+
+def test_error_watch_reports_a_timeout_to_training(cuda_lib):
+    """DeviceErrorWatch and the autograd op: a launch whose wait ran out is reported by a later
+    forward or backward of grouped_det_mm as GdgError(GDG_ETIMEOUT), with no host sync in the
+    op itself; after the report the op runs normally again."""
+    w = wl.Workload("withhold_watch", E=2, N=256, K=256, ops=(), main_grad_std=1.0)
+    h, d = inputs_on(w, DEV, seed=8, sizes=[150, 350], kind=wl.OFFS_ENDS)
+    assert cuda_lib.gdg_device_error() == 0
+
+    # The watch alone: armed behind the timed-out launch, checked once the stream passed it.
+    watch = cuda_lib.DeviceErrorWatch(DEV)
+    watch.check()                                   # nothing armed: nothing to report
+    args, dims, _, keep = cuda_lib._fwd_args(d["X"], d["W"], d["offs"], None, wl.OFFS_ENDS)
+    assert withhold(cuda_lib, cuda_lib.GDG_OP_FWD, args, dims, d["offs"]) == 0
+    watch.arm()
+    torch.cuda.synchronize()
+    del keep
+    with pytest.raises(cuda_lib.GdgError) as err:
+        watch.check()
+    assert err.value.status == GDG_ETIMEOUT
+    watch.check()                                   # reported once
+    assert cuda_lib.gdg_device_error() == 0         # the arm reset the word
+
+    # Through autograd: the backward after the timed-out launch arms the op's watch; the next
+    # forward raises.
+    x = d["X"].clone().requires_grad_(True)
+    wt = d["W"].clone().requires_grad_(True)
+    args, dims, _, keep = cuda_lib._fwd_args(d["X"], d["W"], d["offs"], None, wl.OFFS_ENDS)
+    assert withhold(cuda_lib, cuda_lib.GDG_OP_FWD, args, dims, d["offs"]) == 0
+    y = cuda_lib.grouped_det_mm(x, wt, d["offs"])
+    y.backward(d["G"])
+    torch.cuda.synchronize()
+    del keep
+    with pytest.raises(cuda_lib.GdgError) as err:
+        cuda_lib.grouped_det_mm(x, wt, d["offs"])
+    assert err.value.status == GDG_ETIMEOUT
+    # Reported once; the op then matches the oracle again.
+    y = cuda_lib.grouped_det_mm(x.detach(), wt.detach(), d["offs"])
+    ref = oracle.fwd(h["X"], h["W"], h["offs_np"], wl.OFFS_ENDS)
+    assert_bf16_close(y, ref, "fwd after the reported timeout")
+    torch.cuda.synchronize()
+    assert cuda_lib.gdg_device_error() == 0
